@@ -1,0 +1,92 @@
+// Shared device helpers of the IndexCache kernels (sm_103a).
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace ic {
+
+// Largest k the selection kernels keep; candidate buffers are sized from it.
+constexpr int kMaxK = 2048;
+
+// Device-side error word codes (written by bounded waits that give up).
+constexpr int kDevOk = 0;
+constexpr int kDevTimeout = 1;
+
+// Order-preserving map float -> uint32: a > b  <=>  key(a) > key(b).
+// -0.0 is folded onto +0.0 first so that equal scores compare equal.
+__device__ __forceinline__ uint32_t float_key(float f) {
+  f = (f == 0.0f) ? 0.0f : f;
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_float(uint32_t k) {
+  uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+  return __uint_as_float(u);
+}
+
+// bf16 pair -> two floats (exact).
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t v) {
+  return make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
+// OCP e4m3 byte -> bf16 bits, exactly (every e4m3 value is a bf16 value).
+// Normal codes move the exponent from bias 7 to bias 127 and the 3 mantissa
+// bits to the top of bf16's 7; subnormal codes (exponent field 0) are
+// m * 2^-9 and are built as a float first.
+__device__ __forceinline__ uint32_t e4m3_to_bf16_bits(uint32_t b) {
+  uint32_t s = (b & 0x80u) << 8;
+  uint32_t e = (b >> 3) & 0xFu;
+  uint32_t m = b & 0x7u;
+  if (e == 15u && m == 7u) return s | 0x7FC0u;   // the NaN code stays NaN
+  if (e == 0) {
+    float v = (float)m * (1.0f / 512.0f);
+    return s | (__float_as_uint(v) >> 16);
+  }
+  return s | ((e + 120u) << 7) | (m << 4);
+}
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool pred) {
+  uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+  int n = pred ? 16 : 0;   // src-size 0 fills the 16 bytes with zeros
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" :: "r"(sa), "l"(gmem), "r"(n));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" :: "n"(N)); }
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                            const void* smem) {
+  uint32_t a = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3,
+                                                  const void* smem) {
+  uint32_t a = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(a));
+}
+__device__ __forceinline__ void ldmatrix_x2(uint32_t& r0, uint32_t& r1, const void* smem) {
+  uint32_t a = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(r0), "=r"(r1) : "r"(a));
+}
+
+// D(16x8 f32) += A(16x16 bf16, row) * B(16x8 bf16, col)
+__device__ __forceinline__ void mma_bf16_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+}  // namespace ic

@@ -1,0 +1,42 @@
+// Host-side launchers of the IndexCache kernels (internal to the library).
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ic {
+
+struct IndexerArgs {
+  const void* q;         // [B,T,H,D] bf16
+  const void* kI;        // [B,S_cap,D] bf16 or e4m3
+  const float* kscale;   // [B,S_cap] (e4m3 only)
+  const float* w;        // [B,T,H]
+  int32_t* idx;          // [B,T,k]
+  int B, T, S, S_cap, H, D, k, q_pos0, e4m3;
+};
+
+struct AttnArgs {
+  const void* Q;         // [B,T,Hq,Dh] bf16
+  const void* K;         // [B,S_cap,Dh] bf16
+  const void* V;         // [B,S_cap,Dh] bf16
+  const int32_t* idx;    // [B,T,k]
+  void* O;               // [B,T,Hq,Dh] bf16
+  int B, T, S, S_cap, Hq, Dh, k;
+  float scale;
+};
+
+// Fused prefill indexer + streaming top-k (scores never leave the SM).
+cudaError_t launch_indexer_prefill(const IndexerArgs& a, int* dev_status, cudaStream_t st);
+
+// Decode indexer: score rows into ws, then an exact radix select per row.
+size_t indexer_decode_ws_bytes(int B, int T, int S);
+cudaError_t launch_indexer_decode(const IndexerArgs& a, void* ws, size_t ws_bytes, int* dev_status,
+                                  cudaStream_t st);
+// Rows per sequence at or below which the indexer takes the decode path.
+constexpr int kDecodeMaxT = 8;
+
+// Sparse attention; splits the k rows over CTAs (partials in ws) when few rows.
+size_t attn_ws_bytes(int B, int T, int Hq, int Dh, int k);
+cudaError_t launch_sparse_attn(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
+
+}  // namespace ic

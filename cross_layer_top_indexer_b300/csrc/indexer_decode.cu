@@ -1,0 +1,303 @@
+// Decode indexer: few query rows per sequence against a long key cache.
+//
+// Same score as the prefill kernel (DSA lightning-indexer score used by
+// IndexCache's Full layers; notes page "NLP--IndexCache", "背景 & 问题提出"),
+// but the work is spread over the KEYS: one CTA per (tile of keys, query
+// row), so a handful of query rows still fills the GPU.  Each query row's
+// causal scores are staged in the workspace (one fp32 row per query, O(L),
+// never an L x L matrix), then one CTA per row selects the exact top-k with
+// a most-significant-digit radix select and writes the positions in
+// ascending order.
+#include "ic_common.cuh"
+#include "ic_kernels.h"
+
+namespace ic {
+namespace {
+
+constexpr int DKT = 256;          // keys per scoring CTA (8 warps x 32)
+constexpr int DTHREADS = 256;
+constexpr int HMAX = 64;
+
+template <int D>
+struct DecodeSmem {
+  static constexpr int P = D + 8;
+  __nv_bfloat16 qs[HMAX][P];
+  __nv_bfloat16 ks[DKT][P];
+  float wsm[HMAX];
+  float ksc[DKT];
+};
+
+size_t row_pitch(int S) { return (size_t)((S + 3) / 4) * 4; }
+
+template <int D>
+__global__ void __launch_bounds__(DTHREADS)
+decode_scores_kernel(IndexerArgs a, float* scores, int h_pad, size_t pitch) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  auto& sm = *reinterpret_cast<DecodeSmem<D>*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int row = blockIdx.y;                 // b * T + t
+  const int b = row / a.T, t = row - b * a.T;
+  const int pos = a.q_pos0 + t;
+  const int s0 = blockIdx.x * DKT;
+  if (s0 > pos) return;                       // tile entirely past this row's position
+  const int n_keys = pos + 1;
+
+  {
+    const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(a.q) + (size_t)row * a.H * D;
+    constexpr int CH = D / 8;
+    for (int i = tid; i < h_pad * CH; i += DTHREADS) {
+      const int h = i / CH, c = i % CH;
+      const bool ok = h < a.H;
+      cp_async16(&sm.qs[h][c * 8], ok ? qg + (size_t)h * D + c * 8 : qg, ok);
+    }
+    for (int h = tid; h < HMAX; h += DTHREADS) sm.wsm[h] = h < a.H ? a.w[(size_t)row * a.H + h] : 0.0f;
+  }
+  if (!a.e4m3) {
+    const __nv_bfloat16* kg_ = reinterpret_cast<const __nv_bfloat16*>(a.kI) + (size_t)b * a.S_cap * D;
+    constexpr int CH = D / 8;
+    for (int i = tid; i < DKT * CH; i += DTHREADS) {
+      const int r = i / CH, c = i % CH, s = s0 + r;
+      const bool ok = s < n_keys;
+      cp_async16(&sm.ks[r][c * 8], ok ? kg_ + (size_t)s * D + c * 8 : kg_, ok);
+    }
+    for (int r = tid; r < DKT; r += DTHREADS) sm.ksc[r] = 1.0f;
+  } else {
+    const uint8_t* kg8 = reinterpret_cast<const uint8_t*>(a.kI) + (size_t)b * a.S_cap * D;
+    constexpr int CH = D / 16;
+    for (int i = tid; i < DKT * CH; i += DTHREADS) {
+      const int r = i / CH, c = i % CH, s = s0 + r;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (s < n_keys) v = *reinterpret_cast<const uint4*>(kg8 + (size_t)s * D + c * 16);
+      const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t x = wv[j];
+        o[2 * j] = e4m3_to_bf16_bits(x & 0xFF) | (e4m3_to_bf16_bits((x >> 8) & 0xFF) << 16);
+        o[2 * j + 1] = e4m3_to_bf16_bits((x >> 16) & 0xFF) | (e4m3_to_bf16_bits(x >> 24) << 16);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(&sm.ks[r][c * 16]);
+      dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+    for (int r = tid; r < DKT; r += DTHREADS) {
+      const int s = s0 + r;
+      sm.ksc[r] = s < n_keys ? a.kscale[(size_t)b * a.S_cap + s] : 0.0f;
+    }
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+
+  const int n_tiles_h = h_pad / 8;
+  float acc[2][8][4];
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int n = 0; n < 8; ++n)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[m][n][j] = 0.0f;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    uint32_t af[2][4];
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+      ldmatrix_x4(af[m][0], af[m][1], af[m][2], af[m][3],
+                  &sm.ks[wid * 32 + m * 16 + (lane & 15)][kk * 16 + (lane >> 4) * 8]);
+#pragma unroll
+    for (int np = 0; np < 4; ++np) {
+      if (2 * np < n_tiles_h) {
+        const int mat = lane >> 3;
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4(b0, b1, b2, b3, &sm.qs[np * 16 + (mat >> 1) * 8 + (lane & 7)][kk * 16 + (mat & 1) * 8]);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          mma_bf16_16816(acc[m][2 * np], af[m][0], af[m][1], af[m][2], af[m][3], b0, b1);
+          mma_bf16_16816(acc[m][2 * np + 1], af[m][0], af[m][1], af[m][2], af[m][3], b2, b3);
+        }
+      }
+    }
+  }
+  float* out = scores + (size_t)row * pitch;
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float part = 0.0f;
+#pragma unroll
+      for (int n = 0; n < 8; ++n) {
+        if (n < n_tiles_h) {
+          const int h = n * 8 + 2 * (lane & 3);
+          part = fmaf(sm.wsm[h], fmaxf(acc[m][n][2 * half], 0.0f), part);
+          part = fmaf(sm.wsm[h + 1], fmaxf(acc[m][n][2 * half + 1], 0.0f), part);
+        }
+      }
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      const int r = wid * 32 + m * 16 + half * 8 + (lane >> 2);
+      const int s = s0 + r;
+      if ((lane & 3) == 0 && s < n_keys) out[s] = part * sm.ksc[r];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Exact top-k of one staged score row (one CTA per row).
+// ---------------------------------------------------------------------------
+
+constexpr int STHREADS = 1024;
+constexpr int SWARPS = STHREADS / 32;
+
+__global__ void __launch_bounds__(STHREADS)
+decode_select_kernel(const float* scores, size_t pitch, int32_t* idx, int T, int q_pos0, int k) {
+  __shared__ int whist[SWARPS][256];
+  __shared__ int hist[256];
+  __shared__ int wsum[33];
+  __shared__ int sel_digit, sel_need, sel_done;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int row = blockIdx.x;
+  const int t = row % T;
+  const int n = q_pos0 + t + 1;
+  const float* sc = scores + (size_t)row * pitch;
+  int32_t* out = idx + (size_t)row * k;
+
+  if (n <= k) {
+    for (int j = tid; j < k; j += STHREADS) out[j] = j < n ? j : -1;
+    return;
+  }
+  uint32_t pre_hi = 0, msk_hi = 0, pre_lo = 0, msk_lo = 0;
+  int need = k;
+  for (int pass = 0; pass < 8; ++pass) {
+    const bool hi_word = pass < 4;
+    const int shift = 24 - 8 * (pass & 3);
+    for (int i = lane; i < 256; i += 32) whist[wid][i] = 0;
+    __syncwarp();
+    for (int i = tid; i < n; i += STHREADS) {
+      const uint32_t h = float_key(sc[i]);
+      const uint32_t l = ~(uint32_t)i;
+      if ((h & msk_hi) == pre_hi && (l & msk_lo) == pre_lo)
+        atomicAdd(&whist[wid][((hi_word ? h : l) >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    for (int d = tid; d < 256; d += STHREADS) {
+      int s = 0;
+      for (int w = 0; w < SWARPS; ++w) s += whist[w][d];
+      hist[d] = s;
+    }
+    __syncthreads();
+    if (wid == 0) {
+      int c[8];
+      int s = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) { c[j] = hist[255 - 8 * lane - j]; s += c[j]; }
+      int incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const int excl = incl - s;
+      if (excl < need && need <= incl) {
+        int cum = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (cum + c[j] >= need) {
+            sel_digit = 255 - 8 * lane - j;
+            sel_need = need - cum;
+            sel_done = (c[j] == need - cum);
+            break;
+          }
+          cum += c[j];
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t d = (uint32_t)sel_digit;
+    need = sel_need;
+    const int done = sel_done;
+    if (hi_word) { pre_hi |= d << shift; msk_hi |= 255u << shift; }
+    else         { pre_lo |= d << shift; msk_lo |= 255u << shift; }
+    __syncthreads();
+    if (done) break;
+  }
+  // Ordered write of the k survivors: chunks of STHREADS * 4 positions.
+  int written = 0;
+  for (int c0 = 0; c0 < n; c0 += STHREADS * 4) {
+    int cnt = 0;
+    unsigned f = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = c0 + tid * 4 + j;
+      if (i < n) {
+        const uint32_t mh = float_key(sc[i]) & msk_hi;
+        const uint32_t ml = (~(uint32_t)i) & msk_lo;
+        if (mh > pre_hi || (mh == pre_hi && ml >= pre_lo)) { f |= 1u << j; ++cnt; }
+      }
+    }
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) wsum[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      const int s = wsum[lane];
+      int si = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int v = __shfl_up_sync(0xffffffffu, si, o);
+        if (lane >= o) si += v;
+      }
+      wsum[lane] = si - s;
+      if (lane == 31) wsum[32] = si;
+    }
+    __syncthreads();
+    int off = written + wsum[wid] + incl - cnt;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (f & (1u << j)) {
+        if (off < k) out[off] = c0 + tid * 4 + j;
+        ++off;
+      }
+    written += wsum[32];
+    __syncthreads();
+  }
+}
+
+template <int D>
+cudaError_t launch_scores(const IndexerArgs& a, float* scores, size_t pitch, cudaStream_t st) {
+  const int h_pad = ((a.H + 15) / 16) * 16;
+  const size_t smem = sizeof(DecodeSmem<D>);
+  cudaError_t e = cudaFuncSetAttribute(decode_scores_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  const int max_keys = a.q_pos0 + a.T;          // the last row's causal count
+  dim3 grid((max_keys + DKT - 1) / DKT, a.B * a.T);
+  decode_scores_kernel<D><<<grid, DTHREADS, smem, st>>>(a, scores, h_pad, pitch);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t indexer_decode_ws_bytes(int B, int T, int S) { return (size_t)B * T * row_pitch(S) * sizeof(float); }
+
+cudaError_t launch_indexer_decode(const IndexerArgs& a, void* ws, size_t ws_bytes, int* /*dev_status*/,
+                                  cudaStream_t st) {
+  if (ws_bytes < indexer_decode_ws_bytes(a.B, a.T, a.S)) return cudaErrorInvalidValue;
+  float* scores = reinterpret_cast<float*>(ws);
+  const size_t pitch = row_pitch(a.S);
+  cudaError_t e;
+  switch (a.D) {
+    case 32: e = launch_scores<32>(a, scores, pitch, st); break;
+    case 64: e = launch_scores<64>(a, scores, pitch, st); break;
+    case 128: e = launch_scores<128>(a, scores, pitch, st); break;
+    default: return cudaErrorInvalidValue;
+  }
+  if (e != cudaSuccess) return e;
+  decode_select_kernel<<<a.B * a.T, STHREADS, 0, st>>>(scores, pitch, a.idx, a.T, a.q_pos0, a.k);
+  return cudaGetLastError();
+}
+
+}  // namespace ic

@@ -1,0 +1,352 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Integer-valued inputs must give bit-identical index sets; random inputs are
+held to the tolerance rule in ``parity_util``; attention outputs to a max-abs
+error of 2e-2 against the fp64 oracle evaluated on the GPU's own indices.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from cross_layer_top_indexer_b300 import binding as B
+from cross_layer_top_indexer_b300 import synth
+from tests import parity_util as pu
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    B.load()
+
+
+def _idx64(t):
+    return t.cpu().numpy()
+
+
+# ---------------------------------------------------------------------------
+# The pages' worked example, realised through the real indexer kernels.
+# ---------------------------------------------------------------------------
+
+WORKED_ROWS = [[0.1, 0.9, 0.3, 0.2], [0.2, 0.7, 0.4, 0.1], [0.6, 0.1, 0.5, 0.3], [0.8, 0.1, 0.2, 0.7]]
+
+
+def _worked_layers(T):
+    """Layer l: one indexer head, query row 3 = e_0, key s = 10*score_l[s] e_0, w = 1.
+    Scores of row 3 are then exactly 10x the page's row (integers, exact in bf16)."""
+    D = 32
+    layers = []
+    g = torch.Generator(device="cpu").manual_seed(5)
+    for l in range(4):
+        q = torch.zeros(1, T, 1, D)
+        q[0, 3, 0, 0] = 1.0
+        kI = torch.zeros(1, T, D)
+        for s in range(4):
+            kI[0, s, 0] = round(10 * WORKED_ROWS[l][s])
+        w = torch.ones(1, T, 1)
+        Q = torch.randn(1, T, 4, 64, generator=g)
+        K = torch.randn(1, T, 64, generator=g)
+        V = torch.randn(1, T, 64, generator=g)
+        layers.append(dict(q=q.to(DEV, torch.bfloat16), kI=kI.to(DEV, torch.bfloat16), kscale=None,
+                           w=w.to(DEV), Q=Q.to(DEV, torch.bfloat16), K=K.to(DEV, torch.bfloat16),
+                           V=V.to(DEV, torch.bfloat16)))
+    return layers
+
+
+@pytest.mark.parametrize("T", [16, 4])    # 16 rows: prefill kernel; 4 rows: decode kernels
+def test_worked_example_through_kernels(T):
+    layers = _worked_layers(T)
+    expect_row3 = {"F": [1, 2], "FS": [1, 2], "FSS": [1, 2], "FSSF": [0, 3], "FFF": [0, 2], "FFFF": [0, 3]}
+    for pattern, want in expect_row3.items():
+        cache, calls = B.forward_pattern(pattern, layers[: len(pattern)], k=2)
+        torch.cuda.synchronize()
+        assert calls == pattern.count("F")
+        c = _idx64(cache)[0]
+        assert c[3].tolist() == want, (pattern, c[3])
+        assert c[0].tolist() == [0, -1] and c[1].tolist() == [0, 1]
+    # outputs of the FSSF run: layers 1 and 2 attend over layer 0's indices
+    cache, calls = B.forward_pattern("FSSF", layers, k=2)
+    torch.cuda.synchronize()
+    sel, _ = oracle.schedule_rows(WORKED_ROWS, "FSSF", 2)
+    for l in range(4):
+        idx = torch.full((T, 2), -1, dtype=torch.int32)
+        idx[:3] = torch.tensor([[0, -1], [0, 1], [0, 1]], dtype=torch.int32)
+        idx[3] = torch.from_numpy(sel[l][0])
+        if T > 4:   # rows past 3 have all-zero scores: the lowest positions win
+            idx[4:] = torch.tensor([0, 1], dtype=torch.int32)
+        L = layers[l]
+        pu.check_attention(L["O"][0], L["Q"][0], L["K"][0], L["V"][0], idx, 1.0 / 8.0, rows=range(4))
+
+
+# ---------------------------------------------------------------------------
+# Tiny stack: integer inputs, bit-exact indices.
+# ---------------------------------------------------------------------------
+
+
+def test_tiny_stack_bit_exact():
+    cfg = synth.TINY
+    layers = synth.make_stack(cfg, 1234, DEV)
+    per_layer = {}
+    for l, c in enumerate(cfg.pattern):
+        if c == "F":
+            L = layers[l]
+            idx = B.indexer_topk(L["q"], L["kI"], L["w"], cfg.k)
+            torch.cuda.synchronize()
+            want = oracle.indexer_topk(pu.to_f64(L["q"][0]), pu.to_f64(L["kI"][0]), pu.to_f64(L["w"][0]), cfg.k)
+            got = _idx64(idx)[0]
+            assert np.array_equal(got, want), np.argwhere(got != want)[:5]
+            per_layer[l] = want
+    cache, calls = B.forward_pattern(cfg.pattern, layers, cfg.k)
+    torch.cuda.synchronize()
+    assert calls == cfg.pattern.count("F")
+    assert np.array_equal(_idx64(cache)[0], per_layer[3])
+    f = 0
+    for l, c in enumerate(cfg.pattern):
+        f = l if c == "F" else f
+        L = layers[l]
+        idx = torch.from_numpy(per_layer[f])
+        pu.check_attention(L["O"][0], L["Q"][0], L["K"][0], L["V"][0], idx, cfg.scale)
+
+
+# ---------------------------------------------------------------------------
+# Indexer on random and adversarial inputs (prefill kernel).
+# ---------------------------------------------------------------------------
+
+CASES = [
+    # B, T, S, q_pos0, H, D, k, dist, kdtype
+    (1, 1000, 1000, 0, 64, 128, 64, "normal", "bf16"),       # ragged tail, one compaction
+    (2, 333, 1333, 1000, 64, 128, 256, "normal", "bf16"),    # query chunk at an offset, batch 2
+    (1, 700, 700, 0, 16, 64, 2048, "normal", "bf16"),        # k above every causal count
+    (1, 517, 517, 0, 64, 128, 1, "normal", "bf16"),          # k = 1
+    (1, 3000, 3000, 0, 64, 128, 2048, "normal", "bf16"),     # k = 2048 with compactions
+    (1, 600, 600, 0, 8, 32, 100, "int", "bf16"),             # heavy ties, bit-exact
+    (1, 1500, 1500, 0, 64, 128, 256, "normal", "e4m3"),      # fp8 keys
+    (1, 1029, 1029, 0, 4, 32, 16, "int", "bf16"),            # tiny head shape, ragged
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B%d_T%d_S%d_p%d_H%d_D%d_k%d_%s_%s" % c)
+def test_indexer_prefill_cases(case):
+    Bn, T, S, q_pos0, H, D, k, dist, kd = case
+    cfg = synth.StackConfig("case", 1, "F", Bn, T, S, H, D, k, 4, 64, kd, dist, q_pos0)
+    q, kI, ks, w = synth.make_indexer_inputs(cfg, 0, 77, DEV)
+    idx = B.indexer_topk(q, kI, w, k, q_pos0, kscale=ks, S=S)
+    torch.cuda.synchronize()
+    got = _idx64(idx)
+    stats = {"hit": 0, "tot": 0}
+    for b in range(Bn):
+        pu.check_topk(got[b], pu.to_f64(q[b]), pu.keys_f64(kI[b], None if ks is None else ks[b]),
+                      pu.to_f64(w[b]), k, q_pos0, range(T), exact=(dist == "int"), stats=stats)
+    if dist != "int":
+        pu.check_recall(stats)
+
+
+def test_indexer_monotone_scores_many_compactions():
+    # score grows with position in bf16 steps (with exact ties): every key
+    # beats the threshold, so the candidate list is cut back again and again
+    T, D, k = 2600, 32, 300
+    q = torch.zeros(1, T, 1, D)
+    q[..., 0] = 1.0
+    kI = torch.zeros(1, T, D)
+    kI[0, :, 0] = torch.arange(T, dtype=torch.float32) * 0.01
+    w = torch.ones(1, T, 1)
+    q, kI, w = q.to(DEV, torch.bfloat16), kI.to(DEV, torch.bfloat16), w.to(DEV)
+    idx = B.indexer_topk(q, kI, w, k)
+    torch.cuda.synchronize()
+    pu.check_topk(_idx64(idx)[0], pu.to_f64(q[0]), pu.to_f64(kI[0]), pu.to_f64(w[0]), k, 0, range(T), exact=True)
+
+
+def test_indexer_constant_scores_lowest_positions():
+    T, D, k = 1100, 32, 200
+    q = torch.zeros(1, T, 2, D, device=DEV, dtype=torch.bfloat16)
+    kI = torch.ones(1, T, D, device=DEV, dtype=torch.bfloat16)
+    w = torch.ones(1, T, 2, device=DEV)
+    idx = _idx64(B.indexer_topk(q, kI, w, k))[0]
+    for t in (0, 5, 199, 200, 1099):
+        n = min(k, t + 1)
+        assert idx[t].tolist() == list(range(n)) + [-1] * (k - n)
+
+
+# ---------------------------------------------------------------------------
+# Decode path (few rows): score rows in the workspace + radix select.
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("Bn,T,S,S_cap,q_pos0,k,kd", [
+    (4, 1, 5000, 5000, 4999, 2048, "bf16"),
+    (4, 1, 5000, 5100, 4999, 2048, "e4m3"),
+    (2, 3, 4003, 4100, 4000, 16, "bf16"),
+    (3, 1, 100, 100, 99, 2048, "bf16"),      # fewer causal keys than k
+    (1, 8, 3008, 3008, 3000, 500, "e4m3"),
+])
+def test_indexer_decode_path(Bn, T, S, S_cap, q_pos0, k, kd):
+    cfg = synth.StackConfig("dec", 1, "F", Bn, T, S, 64, 128, k, 32, 128, kd, "normal", q_pos0)
+    q, kI, ks, w = synth.make_indexer_inputs(cfg, 0, 91, DEV, S=S_cap)
+    idx = B.indexer_topk(q, kI, w, k, q_pos0, kscale=ks, S=S)
+    torch.cuda.synchronize()
+    got = _idx64(idx)
+    stats = {"hit": 0, "tot": 0}
+    for b in range(Bn):
+        pu.check_topk(got[b], pu.to_f64(q[b]), pu.keys_f64(kI[b, :S], None if ks is None else ks[b, :S]),
+                      pu.to_f64(w[b]), k, q_pos0, range(T), exact=False, stats=stats)
+    pu.check_recall(stats)
+
+
+def test_decode_matches_prefill_row():
+    # the decode kernels at position p give the prefill kernel's row p
+    cfg = synth.StackConfig("x", 1, "F", 1, 1200, 1200, 64, 128, 128, 32, 128)
+    q, kI, _, w = synth.make_indexer_inputs(cfg, 0, 5, DEV)
+    full = _idx64(B.indexer_topk(q, kI, w, 128))[0]
+    for p in (0, 127, 128, 700, 1199):
+        dec = _idx64(B.indexer_topk(q[:, p:p + 1].contiguous(), kI, w[:, p:p + 1].contiguous(), 128, p, S=p + 1))
+        assert np.array_equal(dec[0, 0], full[p])
+
+
+# ---------------------------------------------------------------------------
+# Sparse attention.
+# ---------------------------------------------------------------------------
+
+
+@pytest.mark.parametrize("Bn,T,S,Hq,Dh,k", [
+    (1, 400, 3000, 32, 128, 2048),   # many rows: one CTA per row
+    (2, 300, 900, 4, 64, 100),
+    (32, 1, 5000, 32, 128, 2048),    # few rows: split over the k rows + merge
+    (3, 2, 700, 16, 64, 333),
+])
+def test_sparse_attention(Bn, T, S, Hq, Dh, k):
+    g = torch.Generator(device=DEV).manual_seed(3)
+    Q = torch.randn(Bn, T, Hq, Dh, device=DEV, generator=g).to(torch.bfloat16)
+    K = torch.randn(Bn, S, Dh, device=DEV, generator=g).to(torch.bfloat16)
+    V = torch.randn(Bn, S, Dh, device=DEV, generator=g).to(torch.bfloat16)
+    idx = torch.stack([torch.stack([torch.randperm(S, device=DEV, generator=g)[:k] for _ in range(T)])
+                       for _ in range(Bn)]).to(torch.int32)
+    # -1 holes, a short row and an empty row
+    idx[:, :, ::7] = -1
+    if T > 1:
+        idx[0, 1, 5:] = -1
+        idx[0, 0, :] = -1
+    O = B.sparse_attn(Q, K, V, idx)
+    torch.cuda.synchronize()
+    for b in range(Bn):
+        pu.check_attention(O[b], Q[b], K[b], V[b], idx[b], 1.0 / math.sqrt(Dh))
+    if T > 1:
+        assert torch.all(O[0, 0] == 0)
+
+
+# ---------------------------------------------------------------------------
+# Whole stacks.
+# ---------------------------------------------------------------------------
+
+
+def _stack_check(cfg, layers, sample_rows, base_seed, q_pos0=0, S=None):
+    """Per-F-layer indices through ic_indexer_topk + the forward through
+    ic_forward_pattern; sampled rows against the oracle."""
+    S = cfg.S if S is None else S
+    per_f = {}
+    stats = {"hit": 0, "tot": 0}
+    for l, c in enumerate(cfg.pattern):
+        if c != "F":
+            continue
+        L = layers[l]
+        idx = B.indexer_topk(L["q"], L["kI"], L["w"], cfg.k, q_pos0, kscale=L["kscale"], S=S)
+        torch.cuda.synchronize()
+        per_f[l] = idx.clone()
+        for b in range(cfg.B):
+            pu.check_topk(_idx64(idx)[b], pu.to_f64(L["q"][b]),
+                          pu.keys_f64(L["kI"][b, :S], None if L["kscale"] is None else L["kscale"][b, :S]),
+                          pu.to_f64(L["w"][b]), cfg.k, q_pos0, sample_rows, exact=(cfg.dist == "int"),
+                          stats=stats)
+    if cfg.dist != "int":
+        pu.check_recall(stats)
+    cache, calls = B.forward_pattern(cfg.pattern, layers, cfg.k, q_pos0, S)
+    torch.cuda.synchronize()
+    assert calls == cfg.pattern.count("F")
+    last_f = max(per_f)
+    assert torch.equal(cache, per_f[last_f])
+    f = 0
+    for l, c in enumerate(cfg.pattern):
+        f = l if c == "F" else f
+        L = layers[l]
+        for b in range(cfg.B):
+            pu.check_attention(L["O"][b], L["Q"][b], L["K"][b, :S], L["V"][b, :S], per_f[f][b], cfg.scale,
+                               rows=sample_rows)
+
+
+def _sample_rows(T, k, n_rand, seed):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, k - 2, k - 1, k, k + 1, T - 2, T - 1]
+    rows = sorted(set([r for r in fixed if 0 <= r < T] + rng.integers(0, T, n_rand).tolist()))
+    return rows
+
+
+def test_short_stack_sampled():
+    cfg = synth.SHORT
+    layers = synth.make_stack(cfg, 2024, DEV)
+    _stack_check(cfg, layers, _sample_rows(cfg.T, cfg.k, 24, 1), 2024)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("kd", ["bf16", "e4m3"])
+def test_prefill32k_full_size_sampled(kd):
+    # the 30B-shaped workload's sizes (L = 32768, H_I = 64, d_I = 128, k = 2048,
+    # 32 query heads of dim 128) and launch configuration, on five of its layers
+    cfg = synth.PREFILL_32K.with_(n_layers=5, pattern="FSSSF", k_dtype=kd)
+    layers = synth.make_stack(cfg, 31337, DEV)
+    _stack_check(cfg, layers, _sample_rows(cfg.T, cfg.k, 10, 2), 31337)
+
+
+@pytest.mark.slow
+def test_decode_full_size_sampled():
+    # 32 sequences at context 131072 (plus the new token), fp8 keys; checks 4 sequences
+    cfg = synth.DECODE.with_(n_layers=2, pattern="FS")
+    S = cfg.S
+    layers = synth.make_stack(cfg, 4242, DEV, T=1, S=S)
+    idx = B.indexer_topk(layers[0]["q"], layers[0]["kI"], layers[0]["w"], cfg.k, cfg.q_pos0,
+                         kscale=layers[0]["kscale"], S=S)
+    torch.cuda.synchronize()
+    got = _idx64(idx)
+    stats = {"hit": 0, "tot": 0}
+    for b in (0, 9, 20, 31):
+        L = layers[0]
+        pu.check_topk(got[b], pu.to_f64(L["q"][b]), pu.keys_f64(L["kI"][b], L["kscale"][b]), pu.to_f64(L["w"][b]),
+                      cfg.k, cfg.q_pos0, [0], exact=False, stats=stats)
+    pu.check_recall(stats)
+    cache, calls = B.forward_pattern(cfg.pattern, layers, cfg.k, cfg.q_pos0, S)
+    torch.cuda.synchronize()
+    assert calls == 1 and torch.equal(cache, idx)
+    for l in range(2):
+        L = layers[l]
+        for b in (0, 31):
+            pu.check_attention(L["O"][b], L["Q"][b], L["K"][b], L["V"][b], idx[b], cfg.scale)
+
+
+@pytest.mark.slow
+def test_long_last_chunk_sampled():
+    # the last 8192-query chunk of the 204800-token prefill, fp8 keys
+    cfg = synth.LONG.with_(n_layers=2, pattern="FS", T=8192)
+    q_pos0 = 204800 - 8192
+    layers = synth.make_stack(cfg, 555, DEV, T=8192, S=204800)
+    _stack_check(cfg, layers, _sample_rows(8192, 0, 6, 3), 555, q_pos0=q_pos0, S=204800)
+
+
+def test_bad_pattern_launches_nothing():
+    cfg = synth.TINY
+    layers = synth.make_stack(cfg, 1, DEV)
+    for L in layers:
+        L["O"] = torch.full_like(L["Q"], 7.0)
+    cache = torch.full((1, cfg.T, cfg.k), 12345, dtype=torch.int32, device=DEV)
+    for bad in ("SSSF", "FSX F"[:4], "FS", "1001"):
+        with pytest.raises(ValueError):
+            B.forward_pattern(bad, layers, cfg.k, index_cache=cache)
+    torch.cuda.synchronize()
+    assert torch.all(cache == 12345)
+    assert all(torch.all(L["O"] == 7.0) for L in layers)
+    B.stream_status()
