@@ -52,6 +52,17 @@ int* device_status_ptr() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
+namespace ic {
+// Message hook for entry points defined in other files of the library.
+ic_status report_error(ic_status st, const char* msg) { return fail(st, "%s", msg); }
+void clear_error() { g_msg[0] = 0; }
+int* device_status() { return device_status_ptr(); }
+}  // namespace ic
+
+namespace {
+
 ic_status check_indexer(int B, int T, int S, int S_cap, int H, int D, int k, int q_pos0, const void* q,
                         const void* kI, int k_dtype, const float* k_scale, const float* w, const void* idx) {
   if (B < 1 || T < 1 || S < 1 || H < 1 || D < 1 || k < 1 || q_pos0 < 0)

@@ -40,3 +40,12 @@ size_t attn_ws_bytes(int B, int T, int Hq, int Dh, int k);
 cudaError_t launch_sparse_attn(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
 
 }  // namespace ic
+
+#include "../../include/indexcache.h"
+
+namespace ic {
+// Shared by the entry points of the library (defined in abi.cu).
+ic_status report_error(ic_status st, const char* msg);
+void clear_error();
+int* device_status();
+}  // namespace ic

@@ -127,6 +127,26 @@ ic_status ic_sparse_attn(int B, int T, int S, int S_cap, int Hq, int Dh, int k,
                          const void* Q, const void* K, const void* V, const int32_t* idx,
                          float scale, void* O, void* ws, size_t ws_bytes, void* stream);
 
+/* ic_indexer_topk for few query rows (T <= 8 per sequence: the decode
+ * path) that allocates nothing and takes no workspace.  The paper has no
+ * counterpart to this call; it exists for callers that cannot call
+ * cudaMalloc where they run the indexer, e.g. a server whose memory manager
+ * owns all free device memory, a plugin without access to its host's
+ * allocator, or a loop that must not take cudaMalloc's implicit device
+ * synchronisation.  The score rows it stages live in a fixed 32 MiB device
+ * array inside the library (held by every GPU that loads it, until exit):
+ * B * T * S * 4 bytes (S rounded up to a multiple of 4) must fit, or the call
+ * returns IC_ERR_UNSUPPORTED; T > 8 also returns IC_ERR_UNSUPPORTED.  The
+ * first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any
+ * stream capture.  All calls share the array: calls whose kernels may
+ * overlap on the GPU race on it and must be ordered by the caller.  Nothing
+ * in it needs to start at zero.  Arguments, results and other errors as for
+ * ic_indexer_topk. */
+ic_status ic_indexer_topk_noalloc(int B, int T, int S, int S_cap, int H, int D, int k, int q_pos0,
+                                  const void* q, const void* kI, int k_dtype, const float* k_scale,
+                                  const float* w, int32_t* idx_out, void* stream);
+
 /* The F/S layer loop (deep-read page, "从 DSA 的成本分解开始"; notes page,
  * "IndexCache 方法").  `pattern` is a NUL-terminated string of n_layers
  * characters, each 'F' or 'S', the first 'F'.  The whole pattern and every
