@@ -413,7 +413,7 @@ def ours_arm(args, world, rank, local):
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
         if os.environ.get("CUDA_VISIBLE_DEVICES") else local
     peaks = load_peaks()
-    cfg = synth.PREFILL_32K
+    cfg = synth.CONFIGS[args.config]
     seed = 1000 + 7919 * rank
     quarter = cfg.pattern
     allf = "F" * cfg.n_layers
@@ -478,8 +478,11 @@ def ours_arm(args, world, rank, local):
     line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": "prefill32k: 47 layers, F at 0,4,..,44 (12 F / 35 S), B=1, L=32768 causal, "
-                                   "H_I=64, d_I=128, bf16 keys, k=2048; 32 q heads / 1 KV head, dim 128, bf16",
+            "config": {"workload": ("prefill32k: 47 layers, F at 0,4,..,44 (12 F / 35 S), B=1, L=32768 causal, "
+                                    "H_I=64, d_I=128, bf16 keys, k=2048; 32 q heads / 1 KV head, dim 128, bf16")
+                       if args.config == "prefill32k" else
+                       ("short: 8 layers FSSSFSSS, B=1, L=8192, H_I=64, d_I=128, bf16 keys, k=2048; "
+                        "32 q heads / 1 KV head, dim 128"),
                        "pattern": quarter, "seq_len": cfg.T, "global_batch": cfg.B * world,
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (per layer q_I 512 MiB, Q 256 MiB; 126 MB L2), no flush"},
@@ -504,6 +507,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--decode-steps", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--config", default="prefill32k", choices=["prefill32k", "short"],
+                    help="prefill32k: the headline 47-layer stack; short: the 8-layer L=8192 stack (profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)
