@@ -113,6 +113,8 @@ ic_status run_indexer(const ic::IndexerArgs& a, void* ws, size_t ws_bytes, cudaS
     if (ws_bytes < need || (need && !ws))
       return fail(IC_ERR_ARG, "workspace of %zu bytes is smaller than the %zu needed", ws_bytes, need);
     e = ic::launch_indexer_decode(a, ws, ws_bytes, status, st);
+  } else if (ic::indexer_prefill_tc_supported(a)) {
+    e = ic::launch_indexer_prefill_tc(a, status, st);
   } else {
     e = ic::launch_indexer_prefill(a, status, st);
   }

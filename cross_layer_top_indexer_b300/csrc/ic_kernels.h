@@ -1,5 +1,6 @@
 // Host-side launchers of the IndexCache kernels (internal to the library).
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -26,7 +27,16 @@ struct AttnArgs {
 };
 
 // Fused prefill indexer + streaming top-k (scores never leave the SM).
+// Tensor-core (tcgen05/TMA) kernel for H = 64, D = 128, bf16 keys:
+bool indexer_prefill_tc_supported(const IndexerArgs& a);
+cudaError_t launch_indexer_prefill_tc(const IndexerArgs& a, int* dev_status, cudaStream_t st);
+// mma.sync kernel for every other supported shape:
 cudaError_t launch_indexer_prefill(const IndexerArgs& a, int* dev_status, cudaStream_t st);
+
+// 2-D TMA map over a row-major [rows, cols] tensor with a [box_rows, box_cols]
+// box (128-byte swizzle when a box row is 128 bytes).
+bool encode_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elt_bytes, uint64_t rows,
+                    uint64_t cols, uint32_t box_rows, uint32_t box_cols);
 
 // Decode indexer: score rows into ws, then an exact radix select per row.
 size_t indexer_decode_ws_bytes(int B, int T, int S);

@@ -1,0 +1,333 @@
+// Fused lightning indexer + streaming top-k on the 5th-generation tensor
+// cores (tcgen05 + TMA + tensor memory), for the production indexer shape
+// H_I = 64 heads, d_I = 128, bf16 keys.
+//
+// Score (DSA lightning-indexer score, the Full layers of IndexCache; notes
+// page "NLP--IndexCache", section "背景 & 问题提出"):
+//     I[t,s] = sum_h w[t,h] * ReLU(q[t,h,:] . kI[s,:]),   s <= pos(t).
+//
+// One CTA owns QPB = 4 consecutive query rows.  Their q rows form the MMA's
+// B operand (N = 4 x 64 = 256 columns, loaded once by TMA); key tiles of
+// 128 rows form the A operand (M = 128, keys on the TMEM lanes), streamed by
+// TMA in K-halves of 64 features through a 4-deep ring.  One thread issues
+// the MMAs into two TMEM accumulators of 128 x 256 fp32 (all 512 columns),
+// so the tensor core fills one while the epilogue drains the other.
+//
+// Warp roles (10 warps):
+//   warp 0     TMA producer (q once, then key half-tiles)
+//   warp 1     TMEM allocator + MMA issuer
+//   warps 2-9  epilogue: two warpgroups; warpgroup g owns query rows 2g and
+//              2g+1.  Thread = one key (its TMEM lane); it reads the 64 head
+//              dot products of each of its two rows, forms the weighted ReLU
+//              sum in registers, and runs the streaming top-k.
+//
+// Streaming top-k (per row, in shared memory): candidates above the
+// threshold tau (the smallest kept score after the last cut) are appended in
+// ascending key position; a key that only ties tau loses to the kept entry,
+// which has a lower position.  When a tile could overflow the list, an exact
+// radix select over (score, -position) cuts it back to the k best, keeping
+// the order, so after the last tile the list is the answer, ascending.
+// The L x L scores never leave the SM.
+//
+// Every wait is bounded: a wait that gives up sets the CTA's abort flag and
+// the device status word; all roles then wind down, wait (bounded) for the
+// MMAs already issued, and release tensor memory before returning.
+#include "ic_common.cuh"
+#include "ic_kernels.h"
+#include "tc_utils.cuh"
+#include "topk_select.cuh"
+
+namespace ic {
+namespace {
+
+constexpr int QPB = 4;                   // query rows per CTA
+constexpr int HH = 64;                   // indexer heads
+constexpr int DD = 128;                  // indexer feature dim
+constexpr int NCOL = QPB * HH;           // MMA N = 256
+constexpr int KT = 128;                  // keys per tile (MMA M)
+constexpr int KSTAGES = 4;               // ring of K-half tiles (16 KB each)
+constexpr int CAP = kMaxK + 512;         // candidate slots per row
+constexpr int WG_THREADS = 128;
+constexpr int SEG = CAP / WG_THREADS;    // 20 entries per thread in a cut
+constexpr int NWARPS = 10;
+constexpr int NTHREADS = NWARPS * 32;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t IDESC = tc::idesc_bf16_f32(KT, NCOL);
+
+struct __align__(1024) TcSmem {
+  uint8_t qb[2][NCOL * 128];             // B operand: two K-halves, 256 rows x 128 B (SW128)
+  uint8_t kst[KSTAGES][KT * 128];        // A operand ring: K-half tiles, 128 rows x 128 B (SW128)
+  float wsm[QPB][HH];
+  float cand_s[QPB][CAP];
+  int cand_p[QPB][CAP];
+  uint64_t full[KSTAGES];
+  uint64_t empty[KSTAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t qfull;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+  int cnt[QPB];
+  uint32_t tau[QPB];
+  int wc[2][2][4];                       // [warpgroup][row][key quarter] insert counts
+  SelectScratch scr[2];
+};
+
+struct WgSync {
+  int id;
+  __device__ __forceinline__ void operator()() const { tc::named_sync(id, WG_THREADS); }
+};
+
+__device__ __forceinline__ void set_abort(TcSmem& sm, int* status) {
+  sm.abort = 1;
+  if (status) atomicExch(status, kDevTimeout);
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                          IndexerArgs a, int n_groups, int* status) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // the dynamic shared window is 1024-aligned for the swizzled operands
+  TcSmem& sm = *reinterpret_cast<TcSmem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = n_groups - 1 - static_cast<int>(blockIdx.x);   // longest causal range first
+  const int b = blockIdx.y;
+  const int t0 = g * QPB;
+  const int nq = min(QPB, a.T - t0);
+  const int pos0 = a.q_pos0 + t0;
+  const int n_keys = pos0 + nq;
+  int32_t* out = a.idx + (static_cast<size_t>(b) * a.T + t0) * a.k;
+
+  if (n_keys <= a.k) {   // every causal position of every row is selected
+    for (int i = tid; i < nq * a.k; i += NTHREADS) {
+      const int qi = i / a.k, j = i - qi * a.k;
+      out[i] = (j <= pos0 + qi) ? j : -1;
+    }
+    return;
+  }
+  const int nt = (n_keys + KT - 1) / KT;
+
+  // ---- set-up ----
+  if (tid == 0) {
+    for (int s = 0; s < KSTAGES; ++s) { tc::mbar_init(&sm.full[s], 1); tc::mbar_init(&sm.empty[s], 1); }
+    for (int s = 0; s < 2; ++s) { tc::mbar_init(&sm.tfull[s], 1); tc::mbar_init(&sm.tempty[s], 8 * 32); }
+    tc::mbar_init(&sm.qfull, 1);
+    tc::mbar_init(&sm.drain, 1);
+    sm.abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (tid < QPB) { sm.cnt[tid] = 0; sm.tau[tid] = 0u; }
+  for (int i = tid; i < QPB * HH; i += NTHREADS) {
+    const int qi = i / HH, h = i % HH;
+    sm.wsm[qi][h] = qi < nq ? a.w[(static_cast<size_t>(b) * a.T + t0 + qi) * HH + h] : 0.0f;
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&sm.tmem_base, TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      tc::tma_prefetch_map(&tm_q);
+      tc::tma_prefetch_map(&tm_k);
+      const int qrow = (b * a.T + t0) * HH;
+      tc::mbar_arrive_expect_tx(&sm.qfull, 2 * NCOL * 128);
+      tc::tma_load_2d(sm.qb[0], &tm_q, &sm.qfull, 0, qrow);
+      tc::tma_load_2d(sm.qb[1], &tm_q, &sm.qfull, 64, qrow);
+      const int krow0 = b * a.S_cap;
+      int issued = 0;
+      for (int it = 0; it < 2 * nt; ++it) {
+        const int s = it % KSTAGES;
+        const uint32_t ph = (it / KSTAGES) & 1;
+        if (!tc::mbar_wait(&sm.empty[s], ph ^ 1, &sm.abort)) { set_abort(sm, status); break; }
+        tc::mbar_arrive_expect_tx(&sm.full[s], KT * 128);
+        tc::tma_load_2d(sm.kst[s], &tm_k, &sm.full[s], (it & 1) * 64, krow0 + (it >> 1) * KT);
+        issued = it + 1;
+      }
+      // no copy of ours may still be landing in shared memory when the CTA exits
+      tc::mbar_wait(&sm.qfull, 0, nullptr);
+      for (int it = (issued > KSTAGES ? issued - KSTAGES : 0); it < issued; ++it)
+        tc::mbar_wait(&sm.full[it % KSTAGES], (it / KSTAGES) & 1, nullptr);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      bool ok = tc::mbar_wait(&sm.qfull, 0, &sm.abort);
+      if (!ok) set_abort(sm, status);
+      const uint32_t qb0 = tc::smem_u32(sm.qb[0]);
+      const uint32_t qb1 = tc::smem_u32(sm.qb[1]);
+      for (int j = 0; ok && j < nt; ++j) {
+        const int acc = j & 1;
+        if (!tc::mbar_wait(&sm.tempty[acc], ((j >> 1) & 1) ^ 1, &sm.abort)) { set_abort(sm, status); break; }
+        tc::tc_fence_after();
+        const uint32_t d_tmem = tmem + acc * NCOL;
+        for (int h = 0; h < 2; ++h) {
+          const int it = 2 * j + h;
+          const int s = it % KSTAGES;
+          if (!tc::mbar_wait(&sm.full[s], (it / KSTAGES) & 1, &sm.abort)) { set_abort(sm, status); ok = false; break; }
+          tc::tc_fence_after();
+          const uint32_t a_base = tc::smem_u32(sm.kst[s]);
+          const uint32_t b_base = h ? qb1 : qb0;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc::mma_f16(d_tmem, tc::sdesc_k_sw128(a_base + kk * 32), tc::sdesc_k_sw128(b_base + kk * 32), IDESC,
+                        (h | kk) != 0);
+          tc::mma_commit(&sm.empty[s]);   // frees the stage once these MMAs are done
+        }
+        if (!ok) break;
+        tc::mma_commit(&sm.tfull[acc]);   // accumulator ready for the epilogue
+      }
+      // every MMA issued so far is complete before tensor memory is released
+      tc::mma_commit(&sm.drain);
+      if (!tc::mbar_wait(&sm.drain, 0, nullptr, 4000000000ull)) set_abort(sm, status);
+    }
+    __syncwarp();
+  } else {
+    // ================= epilogue: scores + streaming top-k =================
+    const int wg = (warp - 2) >> 2;               // warpgroup 0 / 1
+    const int quarter = warp & 3;                 // TMEM lane quarter this warp may read
+    const int key_local = quarter * 32 + lane;
+    const int wtid = tid - 64 - wg * WG_THREADS;  // 0..127 within the warpgroup
+    const WgSync wsync{1 + wg};
+    const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+    const int q0 = 2 * wg;
+
+    bool aborted = false;
+    for (int j = 0; j < nt; ++j) {
+      const int acc = j & 1;
+      bool ok = tc::mbar_wait(&sm.tfull[acc], (j >> 1) & 1, &sm.abort);
+      if (!ok) set_abort(sm, status);
+      // one decision for the whole warpgroup
+      if (tc::named_sync_or(1 + wg, WG_THREADS, !ok || sm.abort)) { aborted = true; break; }
+      tc::tc_fence_after();
+      float score[2];
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {
+        const uint32_t col = tmem + lane_field + acc * NCOL + (q0 + qq) * HH;
+        uint32_t r0[32], r1[32];
+        tc::tmem_ld_x32(col, r0);
+        tc::tmem_ld_x32(col + 32, r1);
+        tc::tmem_wait_ld();
+        const float* wq = sm.wsm[q0 + qq];
+        float s = 0.0f;
+#pragma unroll
+        for (int h = 0; h < 32; h += 4) {
+          const float4 w4 = *reinterpret_cast<const float4*>(wq + h);
+          s = fmaf(w4.x, fmaxf(__uint_as_float(r0[h + 0]), 0.0f), s);
+          s = fmaf(w4.y, fmaxf(__uint_as_float(r0[h + 1]), 0.0f), s);
+          s = fmaf(w4.z, fmaxf(__uint_as_float(r0[h + 2]), 0.0f), s);
+          s = fmaf(w4.w, fmaxf(__uint_as_float(r0[h + 3]), 0.0f), s);
+        }
+#pragma unroll
+        for (int h = 0; h < 32; h += 4) {
+          const float4 w4 = *reinterpret_cast<const float4*>(wq + 32 + h);
+          s = fmaf(w4.x, fmaxf(__uint_as_float(r1[h + 0]), 0.0f), s);
+          s = fmaf(w4.y, fmaxf(__uint_as_float(r1[h + 1]), 0.0f), s);
+          s = fmaf(w4.z, fmaxf(__uint_as_float(r1[h + 2]), 0.0f), s);
+          s = fmaf(w4.w, fmaxf(__uint_as_float(r1[h + 3]), 0.0f), s);
+        }
+        score[qq] = s;
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&sm.tempty[acc]);           // accumulator may be overwritten
+
+      // cut back any list that could overflow during this tile
+#pragma unroll 1
+      for (int qq = 0; qq < 2; ++qq) {
+        const int qi = q0 + qq;
+        const int c = sm.cnt[qi];
+        if (qi < nq && c > CAP - KT) {
+          select_keep_topk<WG_THREADS, SEG>(sm.cand_s[qi], sm.cand_p[qi], c, a.k, &sm.scr[wg], wtid, wsync);
+          if (wtid == 0) { sm.cnt[qi] = a.k; sm.tau[qi] = sm.scr[wg].tau; }
+          wsync();
+        }
+      }
+      // ordered insertion of the keys above tau
+      const int s_pos = j * KT + key_local;
+      bool take[2];
+      unsigned bal[2];
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {
+        const int qi = q0 + qq;
+        take[qq] = qi < nq && s_pos <= pos0 + qi && float_key(score[qq]) > sm.tau[qi];
+        bal[qq] = __ballot_sync(0xffffffffu, take[qq]);
+        if (lane == 0) sm.wc[wg][qq][quarter] = __popc(bal[qq]);
+      }
+      wsync();
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {
+        const int qi = q0 + qq;
+        if (take[qq]) {
+          int off = __popc(bal[qq] & ((1u << lane) - 1u));
+          for (int x = 0; x < quarter; ++x) off += sm.wc[wg][qq][x];
+          const int slot = sm.cnt[qi] + off;
+          sm.cand_s[qi][slot] = score[qq];
+          sm.cand_p[qi][slot] = s_pos;
+        }
+      }
+      wsync();
+      if (wtid < 2) {
+        const int qi = q0 + wtid;
+        sm.cnt[qi] += sm.wc[wg][wtid][0] + sm.wc[wg][wtid][1] + sm.wc[wg][wtid][2] + sm.wc[wg][wtid][3];
+      }
+    }
+    if (!aborted) aborted = tc::named_sync_or(1 + wg, WG_THREADS, sm.abort != 0);
+    // final cut to k and write-out (ascending already)
+    if (!aborted) {
+#pragma unroll 1
+      for (int qq = 0; qq < 2; ++qq) {
+        const int qi = q0 + qq;
+        if (qi >= nq) break;
+        const int c = sm.cnt[qi];
+        if (c > a.k) {
+          select_keep_topk<WG_THREADS, SEG>(sm.cand_s[qi], sm.cand_p[qi], c, a.k, &sm.scr[wg], wtid, wsync);
+          wsync();
+        }
+        const int n = min(c, a.k);
+        int32_t* row = out + static_cast<size_t>(qi) * a.k;
+        for (int x = wtid; x < a.k; x += WG_THREADS) row[x] = x < n ? sm.cand_p[qi][x] : -1;
+      }
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == 1) tc::tmem_dealloc(tmem, TMEM_COLS);
+}
+
+}  // namespace
+
+bool indexer_prefill_tc_supported(const IndexerArgs& a) {
+  return a.H == HH && a.D == DD && !a.e4m3 && a.T > kDecodeMaxT;
+}
+
+cudaError_t launch_indexer_prefill_tc(const IndexerArgs& a, int* dev_status, cudaStream_t st) {
+  CUtensorMap tm_q, tm_k;
+  // q as [B*T*H, 128] bf16 rows, box 256 rows; kI as [B*S_cap, 128], box 128 rows
+  if (!encode_tmap_2d(&tm_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(a.B) * a.T * HH, DD,
+                      NCOL, 64))
+    return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&tm_k, a.kI, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(a.B) * a.S_cap, DD,
+                      KT, 64))
+    return cudaErrorInvalidValue;
+  const int n_groups = (a.T + QPB - 1) / QPB;
+  const size_t smem = sizeof(TcSmem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(indexer_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(n_groups, a.B);
+  indexer_prefill_tc_kernel<<<grid, NTHREADS, smem, st>>>(tm_q, tm_k, a, n_groups, dev_status);
+  return cudaGetLastError();
+}
+
+}  // namespace ic

@@ -20,8 +20,16 @@ struct SelectScratch {
   uint32_t tau;
 };
 
-__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int nthreads, int& total) {
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = nthreads >> 5;
+// Threads of the group are tid = 0 .. nthreads-1 (whole warps); `sync`
+// synchronises exactly that group.
+struct BlockSync {
+  __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+
+template <class Sync>
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int nthreads, int& total, int tid,
+                                                    Sync sync) {
+  const int lane = tid & 31, wid = tid >> 5, nw = nthreads >> 5;
   int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -29,7 +37,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int n
     if (lane >= o) incl += t;
   }
   if (lane == 31) warp_sums[wid] = incl;
-  __syncthreads();
+  sync();
   if (wid == 0) {
     int s = lane < nw ? warp_sums[lane] : 0;
     int si = s;
@@ -41,26 +49,28 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int n
     if (lane < nw) warp_sums[lane] = si - s;   // exclusive prefix of warps
     if (lane == 31) warp_sums[31] = si;        // grand total (nw <= 31)
   }
-  __syncthreads();
+  sync();
   total = warp_sums[31];
   int r = warp_sums[wid] + incl - v;
-  __syncthreads();
+  sync();
   return r;
 }
 
 // Keep the k best of the n candidates (sc[0..n), pos[0..n)), in place and in
 // order; returns through scr->tau the smallest kept float_key.  n > k >= 1.
 // All threads of the block must call it.  SEG = max entries per thread.
-template <int NTHREADS, int SEG>
-__device__ void select_keep_topk(float* sc, int* pos, int n, int k, SelectScratch* scr) {
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+template <int NTHREADS, int SEG, class Sync = BlockSync>
+__device__ void select_keep_topk(float* sc, int* pos, int n, int k, SelectScratch* scr, int tid = -1,
+                                 Sync sync = Sync()) {
+  if (tid < 0) tid = threadIdx.x;
+  const int lane = tid & 31, wid = tid >> 5;
   uint32_t pre_hi = 0, msk_hi = 0, pre_lo = 0, msk_lo = 0;
   int need = k;
   for (int pass = 0; pass < 8; ++pass) {
     const bool hi_word = pass < 4;
     const int shift = 24 - 8 * (pass & 3);
     for (int i = tid; i < 256; i += NTHREADS) scr->hist[i] = 0;
-    __syncthreads();
+    sync();
     for (int i = tid; i < n; i += NTHREADS) {
       uint32_t h = float_key(sc[i]);
       uint32_t l = ~(uint32_t)pos[i];
@@ -69,7 +79,7 @@ __device__ void select_keep_topk(float* sc, int* pos, int n, int k, SelectScratc
         atomicAdd(&scr->hist[d], 1);
       }
     }
-    __syncthreads();
+    sync();
     if (wid == 0) {
       int c[8];
       int s = 0;
@@ -96,13 +106,13 @@ __device__ void select_keep_topk(float* sc, int* pos, int n, int k, SelectScratc
         }
       }
     }
-    __syncthreads();
+    sync();
     const uint32_t dsel = (uint32_t)scr->sel_digit;
     need = scr->sel_need;
     const int done = scr->sel_done;
     if (hi_word) { pre_hi |= dsel << shift; msk_hi |= 255u << shift; }
     else         { pre_lo |= dsel << shift; msk_lo |= 255u << shift; }
-    __syncthreads();
+    sync();
     if (done) break;
   }
   // Ordered compaction: contiguous segment per thread, block scan of counts.
@@ -127,7 +137,7 @@ __device__ void select_keep_topk(float* sc, int* pos, int n, int k, SelectScratc
     }
   }
   int total;
-  int off = block_exclusive_scan(keep, scr->warp_sums, NTHREADS, total);
+  int off = block_exclusive_scan(keep, scr->warp_sums, NTHREADS, total, tid, sync);
   uint32_t local_min = 0xffffffffu;
 #pragma unroll
   for (int j = 0; j < SEG; ++j) {
@@ -145,7 +155,7 @@ __device__ void select_keep_topk(float* sc, int* pos, int n, int k, SelectScratc
     local_min = t < local_min ? t : local_min;
   }
   if (lane == 0 && local_min != 0xffffffffu) atomicMin(&scr->tau, local_min);
-  __syncthreads();
+  sync();
 }
 
 }  // namespace ic

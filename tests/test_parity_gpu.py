@@ -130,6 +130,9 @@ CASES = [
     (1, 600, 600, 0, 8, 32, 100, "int", "bf16"),             # heavy ties, bit-exact
     (1, 1500, 1500, 0, 64, 128, 256, "normal", "e4m3"),      # fp8 keys
     (1, 1029, 1029, 0, 4, 32, 16, "int", "bf16"),            # tiny head shape, ragged
+    (1, 777, 777, 0, 64, 128, 100, "int", "bf16"),           # tensor-core path, integer: bit-exact
+    (2, 2600, 2600, 0, 64, 128, 2048, "int", "bf16"),        # tensor-core path, ties across cuts
+    (1, 4099, 4099, 0, 64, 128, 333, "normal", "bf16"),      # tensor-core path, many cuts, ragged
 ]
 
 
@@ -149,26 +152,28 @@ def test_indexer_prefill_cases(case):
         pu.check_recall(stats)
 
 
-def test_indexer_monotone_scores_many_compactions():
+@pytest.mark.parametrize("H,D", [(1, 32), (64, 128)])    # mma.sync kernel, tensor-core kernel
+def test_indexer_monotone_scores_many_compactions(H, D):
     # score grows with position in bf16 steps (with exact ties): every key
     # beats the threshold, so the candidate list is cut back again and again
-    T, D, k = 2600, 32, 300
-    q = torch.zeros(1, T, 1, D)
-    q[..., 0] = 1.0
+    T, k = 2600, 300
+    q = torch.zeros(1, T, H, D)
+    q[:, :, 0, 0] = 1.0
     kI = torch.zeros(1, T, D)
     kI[0, :, 0] = torch.arange(T, dtype=torch.float32) * 0.01
-    w = torch.ones(1, T, 1)
+    w = torch.ones(1, T, H)
     q, kI, w = q.to(DEV, torch.bfloat16), kI.to(DEV, torch.bfloat16), w.to(DEV)
     idx = B.indexer_topk(q, kI, w, k)
     torch.cuda.synchronize()
     pu.check_topk(_idx64(idx)[0], pu.to_f64(q[0]), pu.to_f64(kI[0]), pu.to_f64(w[0]), k, 0, range(T), exact=True)
 
 
-def test_indexer_constant_scores_lowest_positions():
-    T, D, k = 1100, 32, 200
-    q = torch.zeros(1, T, 2, D, device=DEV, dtype=torch.bfloat16)
+@pytest.mark.parametrize("H,D", [(2, 32), (64, 128)])
+def test_indexer_constant_scores_lowest_positions(H, D):
+    T, k = 1100, 200
+    q = torch.zeros(1, T, H, D, device=DEV, dtype=torch.bfloat16)
     kI = torch.ones(1, T, D, device=DEV, dtype=torch.bfloat16)
-    w = torch.ones(1, T, 2, device=DEV)
+    w = torch.ones(1, T, H, device=DEV)
     idx = _idx64(B.indexer_topk(q, kI, w, k))[0]
     for t in (0, 5, 199, 200, 1099):
         n = min(k, t + 1)

@@ -1,0 +1,43 @@
+"""One bf16 tile through the tensor-core plumbing (TMA with 128-byte swizzle,
+UMMA shared-memory descriptors, tcgen05.mma into tensor memory, tcgen05.ld),
+compared exactly with a matmul of integer-valued operands."""
+
+import ctypes
+import os
+import subprocess
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+
+
+@pytest.fixture(scope="module")
+def probe(tmp_path_factory):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    out = str(tmp_path_factory.mktemp("probe") / "libtcprobe.so")
+    cmd = ["/usr/local/cuda/bin/nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O2", "-std=c++17",
+           "-shared", "-Xcompiler", "-fPIC", "-I", os.path.join(ROOT, "include"),
+           os.path.join(HERE, "cuda", "tc_tile_probe.cu"),
+           os.path.join(ROOT, "cross_layer_top_indexer_b300", "csrc", "tmap.cu"), "-o", out]
+    subprocess.run(cmd, check=True, capture_output=True)
+    lib = ctypes.CDLL(out)
+    lib.tc_tile_probe.argtypes = [ctypes.c_void_p] * 4
+    lib.tc_tile_probe.restype = ctypes.c_int
+    return lib
+
+
+def test_single_tile_matches_matmul(probe):
+    g = torch.Generator(device="cuda").manual_seed(0)
+    A = torch.randint(-3, 4, (128, 128), device="cuda", generator=g).to(torch.bfloat16)
+    Bm = torch.randint(-3, 4, (256, 128), device="cuda", generator=g).to(torch.bfloat16)
+    D = torch.full((128, 256), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = probe.tc_tile_probe(A.data_ptr(), Bm.data_ptr(), D.data_ptr(), st.data_ptr())
+    assert rc == 0 and int(st.item()) == 0, (rc, int(st.item()))
+    want = A.float() @ Bm.float().T
+    assert torch.equal(D, want), (D - want).abs().max()
