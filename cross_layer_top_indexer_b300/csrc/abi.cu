@@ -125,7 +125,7 @@ ic_status run_attn(const ic::AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_
   const size_t need = ic::attn_ws_bytes(a.B, a.T, a.Hq, a.Dh, a.k);
   if (ws_bytes < need || (need && !ws))
     return fail(IC_ERR_ARG, "workspace of %zu bytes is smaller than the %zu needed", ws_bytes, need);
-  cudaError_t e = ic::launch_sparse_attn(a, ws, ws_bytes, st);
+  cudaError_t e = ic::launch_sparse_attn(a, ws, ws_bytes, device_status_ptr(), st);
   return e == cudaSuccess ? IC_OK : cuda_fail(e, "sparse attention launch");
 }
 

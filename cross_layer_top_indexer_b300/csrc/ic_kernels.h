@@ -47,7 +47,10 @@ constexpr int kDecodeMaxT = 8;
 
 // Sparse attention; splits the k rows over CTAs (partials in ws) when few rows.
 size_t attn_ws_bytes(int B, int T, int Hq, int Dh, int k);
-cudaError_t launch_sparse_attn(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st);
+cudaError_t launch_sparse_attn(const AttnArgs& a, void* ws, size_t ws_bytes, int* dev_status, cudaStream_t st);
+// Tensor-core (tcgen05 + TMA gather) kernel for Hq = 32, Dh = 128 and many rows:
+bool sparse_attn_tc_supported(const AttnArgs& a);
+cudaError_t launch_sparse_attn_tc(const AttnArgs& a, int* dev_status, cudaStream_t st);
 
 }  // namespace ic
 

@@ -333,7 +333,8 @@ size_t attn_ws_bytes(int B, int T, int Hq, int Dh, int k) {
   return nsplit > 1 ? (size_t)rows * nsplit * Partial::floats(Dh) * sizeof(float) : 0;
 }
 
-cudaError_t launch_sparse_attn(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t st) {
+cudaError_t launch_sparse_attn(const AttnArgs& a, void* ws, size_t ws_bytes, int* dev_status, cudaStream_t st) {
+  if (sparse_attn_tc_supported(a)) return launch_sparse_attn_tc(a, dev_status, st);
   switch (a.Dh) {
     case 64: return launch_dh<64>(a, ws, ws_bytes, st);
     case 128: return launch_dh<128>(a, ws, ws_bytes, st);

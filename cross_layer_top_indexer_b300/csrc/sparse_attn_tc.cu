@@ -1,0 +1,488 @@
+// Sparse core attention on the 5th-generation tensor cores (tcgen05 +
+// tensor memory), for the production head shape: 32 query heads sharing one
+// K/V head of dim 128, bf16.
+//
+// IndexCache keeps DeepSeek-Sparse-Attention's core attention: each query
+// attends only to its k selected tokens, O(L^2) -> O(Lk) (notes page
+// "NLP--IndexCache", section "背景 & 问题提出").
+//
+//   O[t,h,:] = sum_j softmax_j(scale * Q[t,h,:] . K[idx_j,:]) V[idx_j,:]
+//
+// Every query row gathers its own k K rows and k V rows, so the work per row
+// is a pair of skinny products over gathered operands; the bound is the
+// gather out of L2, and the design keeps as many gathered bytes in flight as
+// shared memory allows.  Keys go on the MMA M axis (128 per tile, TMEM lanes):
+//
+//   S^T[key, h]  = K_tile (M=128 keys, K-major) x Q^T (N=32 heads, K-major)
+//   O^T[d, h]   += V_tile^T (M=128 d, MN-major) x P^T (N=32 heads, MN-major)
+//
+// so the softmax thread that owns key lane j holds that key's 32 head
+// scores, and the output accumulates in TMEM with d on the lanes.
+//
+// Persistent CTAs (one per SM) walk query rows row = blockIdx.x + i*gridDim.x.
+// Warp roles (11 warps):
+//   warps 0-7  softmax + epilogue in two head groups: warps 0-3 own heads
+//              0-15, warps 4-7 heads 16-31 (warp w reads TMEM lane quarter
+//              w % 4); thread = key lane for P, = d lane for O.  Thread 0
+//              also loads Q (TMA tile) and the index row (bulk copy) two
+//              rows ahead into a double buffer.
+//   warp 8     MMA issuer, over the CTA's tiles in one flat sequence:
+//              QK^T of tile g, then PV of tile g-1
+//   warps 9-10 producers: the K rows and the V rows of every tile, gathered
+//              with 16-byte asynchronous copies into a ring of 32 KB slots
+//              (order K0 V0 K1 V1 ...) in the 128-byte-swizzled operand layout.
+//              Every producer thread copies one 16-byte chunk of a quarter of
+//              the rows of every slot; a slot is published (the threads' own
+//              copies waited for and fenced into the async proxy) once LAG
+//              later slots have been issued, so LAG + 1 slots are in flight.
+//
+// Softmax (per head group, the groups never wait on each other): the
+// reference max m_h of a head is raised only when some score of a tile
+// exceeds it by more than kTau (log2 units), so p = 2^(x - m) <= 2^kTau.  The
+// common tile therefore needs no cross-lane reduction at all: one vote says
+// whether any score crossed the threshold.  Only then (and on a row's first
+// tile) is the exact tile maximum reduced across the 128 key lanes, m_h
+// moved, and the group's O columns in TMEM rescaled (after the previous PV
+// finished).  The sum l_h is kept per thread (one partial per key lane) and
+// reduced across the lanes once per row.
+//
+// Every wait is bounded; a wait that gives up sets the CTA's abort flag and
+// the device status word, every role winds down, in-flight MMAs and copies
+// are waited for (bounded), and tensor memory is released before returning.
+#include <math.h>
+
+#include "ic_common.cuh"
+#include "ic_kernels.h"
+#include "tc_utils.cuh"
+
+namespace ic {
+namespace {
+
+constexpr int HQ = 32;                       // query heads (MMA N)
+constexpr int DH = 128;                      // head dim
+constexpr int KT = 128;                      // keys per tile (MMA M of QK^T)
+constexpr int NSLOT = 5;                     // ring slots of 32 KB (a K or a V tile)
+constexpr int SLOT_BYTES = KT * DH * 2;      // 32 KB: two 64-column halves, 128-byte swizzle
+constexpr int HALF_BYTES = SLOT_BYTES / 2;
+constexpr int Q_BYTES = HQ * DH * 2;         // 8 KB
+constexpr int P_BYTES = KT * HQ * 2;         // 8 KB: [key][head] bf16, 64-byte swizzle
+constexpr int HG = 16;                       // heads per softmax group
+constexpr int SOFT_THREADS = 256;            // two groups of 128
+constexpr int GROUP_THREADS = 128;
+constexpr int MMA_WARP = 8;
+constexpr int PROD_WARP0 = 9;
+constexpr int PROD_WARPS = 2;
+constexpr int PROD_THREADS = PROD_WARPS * 32;
+constexpr int PROD_ROWS = KT * 16 / PROD_THREADS;   // rows of a slot each producer thread copies (one chunk each)
+constexpr int LAG = 2;                       // slots issued after a slot before it is published
+constexpr int NTHREADS = (9 + PROD_WARPS) * 32;
+constexpr uint32_t TMEM_COLS = 128;          // S: 2 x 32 columns, O: 2 x 32 columns
+constexpr float kTau = 8.0f;
+constexpr float kMInit = -1.0e30f;           // reference max before any valid key (finite: no inf - inf)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t IDESC_QK = tc::idesc_bf16_f32(KT, HQ);
+constexpr uint32_t IDESC_PV = tc::idesc_bf16_f32(DH, HQ) | (1u << 15) | (1u << 16);   // A and B MN-major
+
+struct __align__(1024) AttnTcSmem {
+  uint8_t ring[NSLOT][SLOT_BYTES];
+  uint8_t qs[2][Q_BYTES];                    // per row buffer: two 64-column halves of 32 x 128 B
+  uint8_t ps[2][P_BYTES];
+  int32_t idx[2][kMaxK];
+  float red[8][HG];                          // per-warp partial max / sum (warp w: group w / 4)
+  float m_ref[HQ];
+  float alpha[HQ];
+  float inv_l[HQ];
+  uint64_t full[NSLOT], empty[NSLOT];
+  uint64_t qfull[2];
+  uint64_t sfull[2], sempty[2];
+  uint64_t pfull[2], pempty[2];
+  uint64_t ofull[2], oempty[2];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void set_abort(AttnTcSmem& sm, int* status) {
+  sm.abort = 1;
+  if (status) atomicExch(status, kDevTimeout);
+}
+
+// Lanes i and i + 16 of the warp end with the maximum (or sum) over all 32
+// lanes of v[i % 16]: exchange steps of 8, 4, 2, 1 values, then one more
+// across the two half-warps.
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce_scatter16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float keep = upper ? v[i + w] : v[i];
+      const float send = upper ? v[i] : v[i + w];
+      const float got = __shfl_xor_sync(0xffffffffu, send, w);
+      v[i] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  const float got = __shfl_xor_sync(0xffffffffu, v[0], 16);
+  return kMax ? fmaxf(v[0], got) : v[0] + got;
+}
+
+// Q rows and the index row of `row` into buffer qb (completion on qfull[qb]).
+__device__ __forceinline__ void load_row_inputs(AttnTcSmem& sm, const CUtensorMap* tm_q, const AttnArgs& a, int row,
+                                                int qb) {
+  tc::mbar_arrive_expect_tx(&sm.qfull[qb], Q_BYTES + a.k * 4);
+  tc::tma_load_2d(sm.qs[qb], tm_q, &sm.qfull[qb], 0, row * HQ);
+  tc::tma_load_2d(sm.qs[qb] + Q_BYTES / 2, tm_q, &sm.qfull[qb], 64, row * HQ);
+  tc::bulk_g2s(sm.idx[qb], a.idx + static_cast<size_t>(row) * a.k, a.k * 4, &sm.qfull[qb]);
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, AttnArgs a, int* status) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  AttnTcSmem& sm = *reinterpret_cast<AttnTcSmem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rows = a.B * a.T;
+  const int k = a.k;
+  const int nt = (k + KT - 1) / KT;
+  // rows of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
+  const int n_rows = rows > static_cast<int>(blockIdx.x)
+                         ? (rows - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+                         : 0;
+  const uint32_t n_tiles = static_cast<uint32_t>(n_rows) * nt;
+
+  if (tid == 0) {
+    for (int s = 0; s < NSLOT; ++s) {
+      tc::mbar_init(&sm.full[s], PROD_THREADS);
+      tc::mbar_init(&sm.empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(&sm.qfull[s], 1);
+      tc::mbar_init(&sm.sfull[s], 1);
+      tc::mbar_init(&sm.sempty[s], SOFT_THREADS);
+      tc::mbar_init(&sm.pfull[s], SOFT_THREADS);
+      tc::mbar_init(&sm.pempty[s], 1);
+      tc::mbar_init(&sm.ofull[s], 1);
+      tc::mbar_init(&sm.oempty[s], SOFT_THREADS);
+    }
+    tc::mbar_init(&sm.drain, 1);
+    sm.abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == MMA_WARP) {
+    tc::tmem_alloc(&sm.tmem_base, TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const uint32_t tS = tmem;          // columns 0..63: S buffers
+  const uint32_t tO = tmem + 64;     // columns 64..127: O buffers
+
+  if (warp >= PROD_WARP0) {
+    // ================= producers =================
+    constexpr int RSTEP = PROD_THREADS / 16;
+    const int pt = tid - PROD_WARP0 * 32;            // 0 .. PROD_THREADS-1
+    const int c = pt & 15;                           // 16-byte chunk of a 256-byte row
+    const int half = c >> 3, cc = c & 7;
+    const int r0 = pt >> 4;                          // rows r0, r0 + RSTEP, ...
+    const __nv_bfloat16* Kg = reinterpret_cast<const __nv_bfloat16*>(a.K) + c * 8;
+    const __nv_bfloat16* Vg = reinterpret_cast<const __nv_bfloat16*>(a.V) + c * 8;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int n = 0; ok && n < n_rows; ++n) {
+      const int row = static_cast<int>(blockIdx.x) + n * static_cast<int>(gridDim.x);
+      const int qb = n & 1;
+      if (!tc::mbar_wait(&sm.qfull[qb], (n >> 1) & 1, &sm.abort)) { ok = false; break; }
+      const size_t base_row = static_cast<size_t>(row / a.T) * a.S_cap;
+      for (int j = 0; ok && j < nt; ++j) {
+        int src[PROD_ROWS];
+        const int32_t* irow = sm.idx[qb] + j * KT;
+        const int lim = k - j * KT;                  // positions past k are empty slots
+#pragma unroll
+        for (int i = 0; i < PROD_ROWS; ++i) {
+          const int r = r0 + RSTEP * i;
+          const int s = r < lim ? irow[r] : -1;
+          src[i] = (s >= 0 && s < a.S) ? s : 0;      // an empty slot reads row 0 (masked later)
+        }
+#pragma unroll 1
+        for (int kv = 0; kv < 2; ++kv, ++it) {
+          const int slot = static_cast<int>(it % NSLOT);
+          if (!tc::mbar_wait(&sm.empty[slot], ((it / NSLOT) & 1) ^ 1, &sm.abort)) { ok = false; break; }
+          const __nv_bfloat16* base = (kv ? Vg : Kg) + base_row * DH;
+          uint8_t* dst = sm.ring[slot] + half * HALF_BYTES;
+#pragma unroll
+          for (int i = 0; i < PROD_ROWS; ++i) {
+            const int r = r0 + RSTEP * i;
+            cp_async16(dst + r * 128 + ((cc ^ (r & 7)) << 4), base + static_cast<size_t>(src[i]) * DH, true);
+          }
+          cp_async_commit();
+          if (it >= LAG) {
+            // the slot issued LAG slots ago has landed: publish it to the tensor core
+            cp_async_wait<LAG>();
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(&sm.full[(it - LAG) % NSLOT]);
+          }
+        }
+      }
+    }
+    // publish (or, after an abort, just wait out) the last slots in flight
+    cp_async_wait<0>();
+    tc::fence_proxy_async_smem();
+    for (uint32_t i = (it > LAG ? it - LAG : 0); i < it; ++i) tc::mbar_arrive(&sm.full[i % NSLOT]);
+    if (!ok) set_abort(sm, status);
+  } else if (warp == MMA_WARP) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      bool ok = true;
+      for (uint32_t g = 0; ok && g <= n_tiles; ++g) {
+        if (g < n_tiles) {
+          // S^T(g) = K_g Q^T
+          const int n = static_cast<int>(g / nt);
+          const int j = static_cast<int>(g % nt);
+          const int qb = n & 1;
+          const int sb = g & 1;
+          const uint32_t itk = 2 * g;
+          const int slot = static_cast<int>(itk % NSLOT);
+          if (j == 0 && !tc::mbar_wait(&sm.qfull[qb], (n >> 1) & 1, &sm.abort)) { ok = false; break; }
+          if (!tc::mbar_wait(&sm.sempty[sb], ((g >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
+          if (!tc::mbar_wait(&sm.full[slot], (itk / NSLOT) & 1, &sm.abort)) { ok = false; break; }
+          tc::tc_fence_after();
+          const uint32_t kb = tc::smem_u32(sm.ring[slot]);
+          const uint32_t q0 = tc::smem_u32(sm.qs[qb]);
+#pragma unroll
+          for (int kk = 0; kk < DH / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
+            const uint32_t qoff = (kk >> 2) * (Q_BYTES / 2) + (kk & 3) * 32;
+            tc::mma_f16(tS + sb * HQ, tc::sdesc_k_sw128(kb + off), tc::sdesc_k_sw128(q0 + qoff), IDESC_QK, kk != 0);
+          }
+          tc::mma_commit(&sm.empty[slot]);
+          tc::mma_commit(&sm.sfull[sb]);
+        }
+        if (g > 0) {
+          // O^T += V_{g-1}^T P_{g-1}^T
+          const uint32_t gp = g - 1;
+          const int n = static_cast<int>(gp / nt);
+          const int j = static_cast<int>(gp % nt);
+          const int ob = n & 1;
+          const int pb = gp & 1;
+          const uint32_t itv = 2 * gp + 1;
+          const int slot = static_cast<int>(itv % NSLOT);
+          if (j == 0 && !tc::mbar_wait(&sm.oempty[ob], ((n >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
+          if (!tc::mbar_wait(&sm.full[slot], (itv / NSLOT) & 1, &sm.abort)) { ok = false; break; }
+          if (!tc::mbar_wait(&sm.pfull[pb], (gp >> 1) & 1, &sm.abort)) { ok = false; break; }
+          tc::tc_fence_after();
+          const uint32_t vb = tc::smem_u32(sm.ring[slot]);
+          const uint32_t pbase = tc::smem_u32(sm.ps[pb]);
+#pragma unroll
+          for (int kk = 0; kk < KT / 16; ++kk)
+            tc::mma_f16(tO + ob * HQ, tc::sdesc(vb + kk * 2048, HALF_BYTES, 1024, 2),
+                        tc::sdesc(pbase + kk * 1024, 0, 512, 4), IDESC_PV, (j > 0 || kk != 0) ? 1u : 0u);
+          tc::mma_commit(&sm.empty[slot]);
+          tc::mma_commit(&sm.pempty[pb]);
+          if (j == nt - 1) tc::mma_commit(&sm.ofull[ob]);
+        }
+      }
+      if (!ok) set_abort(sm, status);
+      // every MMA issued so far is complete before tensor memory is released
+      tc::mma_commit(&sm.drain);
+      if (!tc::mbar_wait(&sm.drain, 0, nullptr, 4000000000ull)) set_abort(sm, status);
+    }
+    __syncwarp();
+  } else {
+    // ================= softmax + epilogue (warps 0-7, two head groups) =================
+    const int grp = warp >> 2;                     // heads 16*grp .. 16*grp + 15
+    const int gw = warp & 3;                       // warp within the group = TMEM lane quarter
+    const int bar_id = 1 + grp;
+    const int my_lane = gw * 32 + lane;            // key lane (S, P) and d lane (O)
+    const uint32_t lane_field = static_cast<uint32_t>(gw * 32) << 16;
+    const int h0 = grp * HG;
+    const float sl2 = a.scale * kLog2e;
+    if (tid == 0) {
+      tc::tma_prefetch_map(&tm_q);
+      for (int n = 0; n < 2 && n < n_rows; ++n)
+        load_row_inputs(sm, &tm_q, a, static_cast<int>(blockIdx.x) + n * static_cast<int>(gridDim.x), n);
+    }
+    uint32_t g = 0;
+    bool ok = true;
+    for (int n = 0; ok && n < n_rows; ++n) {
+      const int row = static_cast<int>(blockIdx.x) + n * static_cast<int>(gridDim.x);
+      const int qb = n & 1;
+      if (!tc::mbar_wait(&sm.qfull[qb], (n >> 1) & 1, &sm.abort)) ok = false;
+      if (tc::named_sync_or(bar_id, GROUP_THREADS, !ok || sm.abort)) { ok = false; break; }
+      float lp[HG], mr[HG];
+#pragma unroll
+      for (int h = 0; h < HG; ++h) { lp[h] = 0.0f; mr[h] = kMInit; }
+      for (int j = 0; j < nt; ++j, ++g) {
+        const int sb = g & 1;
+        bool w_ok = tc::mbar_wait(&sm.sfull[sb], (g >> 1) & 1, &sm.abort);
+        if (tc::named_sync_or(bar_id, GROUP_THREADS, !w_ok || sm.abort)) { ok = false; break; }
+        tc::tc_fence_after();
+        uint32_t r[HG];
+        tc::tmem_ld_x16(tS + sb * HQ + h0 + lane_field, r);
+        tc::tmem_wait_ld();
+        tc::tc_fence_before();
+        tc::mbar_arrive(&sm.sempty[sb]);
+        const int kj = j * KT + my_lane;
+        const int sidx = kj < k ? sm.idx[qb][kj] : -1;
+        const bool valid = sidx >= 0 && sidx < a.S;
+        const float sv = valid ? sl2 : 0.0f;       // an empty slot scores -inf: 0 * s - inf
+        const float ov = valid ? 0.0f : -INFINITY;
+        // exponent t = s * scale * log2(e) - m for every head; a tile whose t
+        // stays <= kTau everywhere needs no change of the reference max
+        float t[HG];
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+          t[h] = fmaf(__uint_as_float(r[h]), sv, ov - mr[h]);
+          tmax = fmaxf(tmax, t[h]);
+        }
+        const bool slow = tc::named_sync_or(bar_id, GROUP_THREADS, j == 0 || tmax > kTau);
+        if (slow) {
+          // exact tile maximum per head of the group, across the 128 key lanes
+          {
+            float y[HG];
+#pragma unroll
+            for (int h = 0; h < HG; ++h) y[h] = fmaf(__uint_as_float(r[h]), sv, ov);   // s*scale*log2(e) or -inf
+            sm.red[warp][lane & 15] = warp_reduce_scatter16<true>(y, lane);
+          }
+          tc::named_sync(bar_id, GROUP_THREADS);
+          if (gw == 0 && lane < HG) {
+            const float* rd = &sm.red[grp * 4][0];
+            const float mt = fmaxf(fmaxf(rd[lane], rd[HG + lane]), fmaxf(rd[2 * HG + lane], rd[3 * HG + lane]));
+            const float mo = j == 0 ? kMInit : sm.m_ref[h0 + lane];
+            const float mn = fmaxf(mo, mt);
+            sm.alpha[h0 + lane] = exp2f(mo - mn);
+            sm.m_ref[h0 + lane] = mn;
+          }
+          tc::named_sync(bar_id, GROUP_THREADS);
+#pragma unroll
+          for (int h = 0; h < HG; ++h) {
+            const float mn = sm.m_ref[h0 + h];
+            t[h] = fmaf(__uint_as_float(r[h]), sv, ov) - mn;
+            mr[h] = mn;
+            lp[h] *= sm.alpha[h0 + h];
+          }
+          if (j > 0) {
+            // this group's O columns hold tiles 0 .. j-1 once PV(g-1) is done: scale them in place
+            const uint32_t gp = g - 1;
+            w_ok = tc::mbar_wait(&sm.pempty[gp & 1], (gp >> 1) & 1, &sm.abort);
+            if (tc::named_sync_or(bar_id, GROUP_THREADS, !w_ok || sm.abort)) { ok = false; break; }
+            tc::tc_fence_after();
+            uint32_t o[HG];
+            const uint32_t taddr = tO + qb * HQ + h0 + lane_field;
+            tc::tmem_ld_x16(taddr, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < HG; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * sm.alpha[h0 + h]);
+            tc::tmem_st_x16(taddr, o);
+            tc::tmem_wait_st();
+          }
+        }
+        // P buffer free once PV(g-2) is done
+        const int pb = g & 1;
+        w_ok = tc::mbar_wait(&sm.pempty[pb], ((g >> 1) & 1) ^ 1, &sm.abort);
+        if (tc::named_sync_or(bar_id, GROUP_THREADS, !w_ok || sm.abort)) { ok = false; break; }
+        uint32_t pk[HG / 2];
+#pragma unroll
+        for (int h = 0; h < HG; h += 2) {
+          const float p0 = tc::ex2_approx(t[h]);
+          const float p1 = tc::ex2_approx(t[h + 1]);
+          lp[h] += p0;
+          lp[h + 1] += p1;
+          pk[h / 2] = pack_bf16x2(p0, p1);
+        }
+        // row my_lane of P: 64 bytes, 16-byte chunk c at (c ^ ((row >> 1) & 3)) (64-byte swizzle);
+        // this group writes chunks 2*grp and 2*grp + 1
+        uint8_t* prow = sm.ps[pb] + my_lane * 64;
+        const int sx = (my_lane >> 1) & 3;
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int c = 2 * grp + c2;
+          *reinterpret_cast<uint4*>(prow + ((c ^ sx) << 4)) =
+              make_uint4(pk[4 * c2], pk[4 * c2 + 1], pk[4 * c2 + 2], pk[4 * c2 + 3]);
+        }
+        tc::fence_proxy_async_smem();
+        tc::tc_fence_before();
+        tc::mbar_arrive(&sm.pfull[pb]);
+      }
+      if (!ok) break;
+      // ---- row epilogue: l_h, then O / l_h as bf16 ----
+      sm.red[warp][lane & 15] = warp_reduce_scatter16<false>(lp, lane);
+      tc::named_sync(bar_id, GROUP_THREADS);
+      if (gw == 0 && lane < HG) {
+        const float* rd = &sm.red[grp * 4][0];
+        const float l = rd[lane] + rd[HG + lane] + rd[2 * HG + lane] + rd[3 * HG + lane];
+        sm.inv_l[h0 + lane] = l > 0.0f ? 1.0f / l : 0.0f;
+      }
+      bool w_ok = tc::mbar_wait(&sm.ofull[qb], (n >> 1) & 1, &sm.abort);
+      if (tc::named_sync_or(bar_id, GROUP_THREADS, !w_ok || sm.abort)) { ok = false; break; }
+      tc::tc_fence_after();
+      uint32_t o[HG];
+      tc::tmem_ld_x16(tO + qb * HQ + h0 + lane_field, o);
+      tc::tmem_wait_ld();
+      tc::tc_fence_before();
+      tc::mbar_arrive(&sm.oempty[qb]);
+      // Q and the index row of row n are no longer read by anyone (both groups
+      // passed their last tile, the MMA's last QK^T of the row is complete):
+      // load row n + 2 into the buffer
+      if (n + 2 < n_rows) {
+        tc::named_sync(3, SOFT_THREADS);
+        if (tid == 0) load_row_inputs(sm, &tm_q, a, row + 2 * static_cast<int>(gridDim.x), qb);
+      }
+      __nv_bfloat16* Ob = reinterpret_cast<__nv_bfloat16*>(a.O) + static_cast<size_t>(row) * HQ * DH +
+                          static_cast<size_t>(h0) * DH + my_lane;
+#pragma unroll
+      for (int h = 0; h < HG; ++h) Ob[h * DH] = __float2bfloat16_rn(__uint_as_float(o[h]) * sm.inv_l[h0 + h]);
+    }
+    if (!ok) set_abort(sm, status);
+    // no row-input copy of ours may still be landing when the CTA exits
+    if (tid == 0 && n_rows > 0) {
+      const int last = n_rows - 1;
+      tc::mbar_wait(&sm.qfull[last & 1], (last >> 1) & 1, nullptr);
+      if (last >= 1) tc::mbar_wait(&sm.qfull[(last - 1) & 1], ((last - 1) >> 1) & 1, nullptr);
+    }
+  }
+
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  if (warp == MMA_WARP) tc::tmem_dealloc(tmem, TMEM_COLS);
+}
+
+}  // namespace
+
+bool sparse_attn_tc_supported(const AttnArgs& a) {
+  // k > KT: a row spans at least two tiles, so the slots a producer still
+  // holds back at a row boundary all belong to the current row
+  return a.Hq == HQ && a.Dh == DH && (a.k % 4) == 0 && a.k > KT && static_cast<long long>(a.B) * a.T >= 2 * 148 &&
+         static_cast<long long>(a.B) * a.T * HQ < (1ll << 31) && static_cast<long long>(a.B) * a.S_cap < (1ll << 31);
+}
+
+cudaError_t launch_sparse_attn_tc(const AttnArgs& a, int* dev_status, cudaStream_t st) {
+  CUtensorMap tm_q, tm_k, tm_v;
+  const uint64_t rows = static_cast<uint64_t>(a.B) * a.T;
+  if (!encode_tmap_2d(&tm_q, a.Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows * HQ, DH, HQ, 64))
+    return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&tm_k, a.K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(a.B) * a.S_cap, DH, 1,
+                      64))
+    return cudaErrorInvalidValue;
+  if (!encode_tmap_2d(&tm_v, a.V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(a.B) * a.S_cap, DH, 1,
+                      64))
+    return cudaErrorInvalidValue;
+  int dev = 0, n_sm = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  const size_t smem = sizeof(AttnTcSmem) + 1024;
+  cudaError_t e = cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const int grid = static_cast<int>(rows < static_cast<uint64_t>(n_sm) ? rows : n_sm);
+  sparse_attn_tc_kernel<<<grid, NTHREADS, smem, st>>>(tm_q, tm_k, tm_v, a, dev_status);
+  return cudaGetLastError();
+}
+
+}  // namespace ic

@@ -2,9 +2,10 @@
 //   * TMA tile::gather4 of 128 arbitrary rows (two 64-column halves, 128 B swizzle)
 //   * S[128 keys x 32] = Kg . Q^T   (A = gathered rows, K-major; B = Q, K-major)
 //   * D[128 d x 32]   = Kg^T . P    (A = gathered rows read MN-major; B = P [keys][32], MN-major, 64 B swizzle)
-// The MN-major product is run with two descriptor variants (leading / stride
-// byte offsets as expected, and swapped) so the test can report which one the
-// hardware follows.  Every variant's addresses stay inside the operand regions.
+// The MN-major descriptors are the ones the sparse-attention kernel uses:
+// A: leading byte offset = the distance between the two 64-column halves,
+// stride byte offset = 1024 (8 rows of 128 B); B: stride byte offset = 512
+// (8 rows of 64 B).
 #include <cuda_bf16.h>
 
 #include "../../cross_layer_top_indexer_b300/csrc/ic_kernels.h"
@@ -84,12 +85,9 @@ __global__ void __launch_bounds__(128, 1) attn_probe_kernel(const __grid_constan
                   (h | kk) != 0);
       // D = Kg^T . P  (MN-major both, M=128 (d), N=32, K=128 keys)
       const uint32_t id_pv = idesc_bf16_f32(128, 32) | (1u << 15) | (1u << 16);
-      const uint32_t lboA[2] = {16384, 1024}, sboA[2] = {1024, 16384};
-      const uint32_t lboB[2] = {8192, 512}, sboB[2] = {512, 8192};
-      for (int v = 0; v < 2; ++v)
-        for (int kk = 0; kk < 8; ++kk)
-          mma_f16(tmem + 32 + 32 * v, make_desc(a0 + kk * 2048, lboA[v], sboA[v], 2),
-                  make_desc(p0 + kk * 1024, lboB[v], sboB[v], 4), id_pv, kk != 0);
+      for (int kk = 0; kk < 8; ++kk)
+        mma_f16(tmem + 32, make_desc(a0 + kk * 2048, 16384, 1024, 2), make_desc(p0 + kk * 1024, 0, 512, 4), id_pv,
+                kk != 0);
       mma_commit(&sm.done);
     }
   }
@@ -97,14 +95,14 @@ __global__ void __launch_bounds__(128, 1) attn_probe_kernel(const __grid_constan
   __syncthreads();
   if (!mbar_wait(&sm.done, 0, nullptr)) { if (tid == 0) *status = 2; }
   tc_fence_after();
-  for (int c = 0; c < 96; c += 32) {
+  for (int c = 0; c < 64; c += 32) {
     uint32_t r[32];
     tmem_ld_x32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c, r);
     tmem_wait_ld();
     const int row = warp * 32 + (tid & 31);
     for (int j = 0; j < 32; ++j) {
       if (c == 0) S[row * 32 + j] = __uint_as_float(r[j]);
-      else Dv[((c / 32 - 1) * 128 + row) * 32 + j] = __uint_as_float(r[j]);
+      else Dv[row * 32 + j] = __uint_as_float(r[j]);
     }
   }
   tc_fence_before();

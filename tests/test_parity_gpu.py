@@ -246,6 +246,51 @@ def test_sparse_attention(Bn, T, S, Hq, Dh, k):
         assert torch.all(O[0, 0] == 0)
 
 
+def _attn_case(Bn, T, S, S_cap, k, mode, seed):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    Q = torch.randn(Bn, T, 32, 128, device=DEV, generator=g)
+    K = torch.randn(Bn, S_cap, 128, device=DEV, generator=g)
+    V = torch.randn(Bn, S_cap, 128, device=DEV, generator=g)
+    idx = torch.stack([torch.stack([torch.sort(torch.randperm(S, device=DEV, generator=g)[:k]).values
+                                    for _ in range(T)]) for _ in range(Bn)]).to(torch.int32)
+    if mode == "growing":
+        # key magnitude grows with position: later tiles beat the running max by
+        # far more than the lazy-rescale threshold, again and again
+        K = K * torch.linspace(0.05, 4.0, S_cap, device=DEV)[None, :, None]
+    elif mode == "spike":
+        # one late key aligned with every head's query dominates the softmax
+        sel = idx[:, :, -1].long()
+        for b in range(Bn):
+            K[b, sel[b]] = Q[b].mean(1) * 6.0
+    elif mode == "masked_head":
+        # the first tile of every row is empty, the rest valid, some rows empty
+        idx[:, :, :128] = -1
+        idx[:, ::9, :] = -1
+        idx[:, 1::5, 200:260] = S + 7    # outside [0, S): empty slots too
+    return Q.to(torch.bfloat16), K.to(torch.bfloat16), V.to(torch.bfloat16), idx
+
+
+@pytest.mark.parametrize("Bn,T,S,S_cap,k,mode", [
+    (1, 296, 5000, 5000, 2048, "normal"),     # tensor-core path at its smallest row count
+    (2, 200, 3000, 3100, 300, "normal"),      # k not a multiple of the 128-key tile, S_cap > S
+    (1, 400, 6000, 6000, 2048, "growing"),    # the reference max rises tile after tile
+    (1, 300, 4000, 4000, 1024, "spike"),      # one dominant late key
+    (2, 160, 3000, 3000, 512, "masked_head"), # leading empty tile, empty rows, out-of-range slots
+])
+def test_sparse_attention_tensor_core_cases(Bn, T, S, S_cap, k, mode):
+    Q, K, V, idx = _attn_case(Bn, T, S, S_cap, k, mode, 11)
+    O = B.sparse_attn(Q, K, V, idx, S=S)
+    torch.cuda.synchronize()
+    B.stream_status()
+    rows = sorted(set([0, 1, 2, T - 1] + list(range(3, T, max(1, T // 40)))))
+    # the C ABI treats any index outside [0, S) as an empty slot, i.e. as -1
+    idx_o = torch.where((idx >= 0) & (idx < S), idx, torch.full_like(idx, -1))
+    for b in range(Bn):
+        pu.check_attention(O[b], Q[b], K[b, :S], V[b, :S], idx_o[b], 1.0 / math.sqrt(128), rows=rows)
+    if mode == "masked_head":
+        assert torch.all(O[:, ::9] == 0)
+
+
 # ---------------------------------------------------------------------------
 # Whole stacks.
 # ---------------------------------------------------------------------------
