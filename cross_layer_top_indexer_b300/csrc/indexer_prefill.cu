@@ -200,7 +200,8 @@ indexer_prefill_kernel(IndexerArgs a, int n_groups, int h_pad) {
     for (int qi = 0; qi < nq; ++qi) {
       const int c = sm.cnt[qi];
       if (c > CAP - KT) {
-        select_keep_topk<NTHREADS, SEG>(sm.cand_s[qi], sm.cand_p[qi], c, a.k, &sm.scr);
+        select_keep_topk<NTHREADS, SEG>(sm.cand_s[qi], sm.cand_p[qi], c, a.k, &sm.scr, tid, BlockSync(),
+                                        sm.tau[qi], 0xFFFFFFFFu, static_cast<uint32_t>(pos0 + qi));
         if (tid == 0) { sm.cnt[qi] = a.k; sm.tau[qi] = sm.scr.tau; }
         __syncthreads();
       }
@@ -241,7 +242,8 @@ indexer_prefill_kernel(IndexerArgs a, int n_groups, int h_pad) {
   for (int qi = 0; qi < nq; ++qi) {
     const int c = sm.cnt[qi];
     if (c > a.k) {
-      select_keep_topk<NTHREADS, SEG>(sm.cand_s[qi], sm.cand_p[qi], c, a.k, &sm.scr);
+      select_keep_topk<NTHREADS, SEG>(sm.cand_s[qi], sm.cand_p[qi], c, a.k, &sm.scr, tid, BlockSync(),
+                                      sm.tau[qi], 0xFFFFFFFFu, static_cast<uint32_t>(pos0 + qi));
       if (tid == 0) sm.cnt[qi] = a.k;
       __syncthreads();
     }

@@ -9,7 +9,7 @@
 // One CTA owns QPB = 4 consecutive query rows.  Their q rows form the MMA's
 // B operand (N = 4 x 64 = 256 columns, loaded once by TMA); key tiles of
 // 128 rows form the A operand (M = 128, keys on the TMEM lanes), streamed by
-// TMA in K-halves of 64 features through a 4-deep ring.  One thread issues
+// TMA in K-halves of 64 features through a 3-deep ring.  One thread issues
 // the MMAs into two TMEM accumulators of 128 x 256 fp32 (all 512 columns),
 // so the tensor core fills one while the epilogue drains the other.
 //
@@ -21,13 +21,19 @@
 //              dot products of each of its two rows, forms the weighted ReLU
 //              sum in registers, and runs the streaming top-k.
 //
-// Streaming top-k (per row, in shared memory): candidates above the
-// threshold tau (the smallest kept score after the last cut) are appended in
-// ascending key position; a key that only ties tau loses to the kept entry,
-// which has a lower position.  When a tile could overflow the list, an exact
-// radix select over (score, -position) cuts it back to the k best, keeping
-// the order, so after the last tile the list is the answer, ascending.
-// The L x L scores never leave the SM.
+// Streaming top-k (per row, in shared memory): a candidate list of (key,
+// position), key = an order-preserving integer image of the score, kept in
+// ascending position order.  A key enters iff it is above the row's
+// threshold tau; keys arrive in ascending position, so a key that only ties
+// tau loses to k kept candidates with lower positions.  The four warps of a
+// warpgroup each own a quarter of a tile's keys; they exchange their
+// per-row insert counts at the one barrier of each tile and append in order,
+// so no other synchronisation is needed.  When a tile would overflow the
+// list, the list is cut: every candidate below a threshold found with a
+// most-significant-digit histogram (at least k kept) is dropped, in order,
+// and tau rises to that threshold.  After the last tile an exact cut to k
+// (ties to the lower position) leaves the answer, already ascending.  The
+// L x L scores never leave the SM.
 //
 // Every wait is bounded: a wait that gives up sets the CTA's abort flag and
 // the device status word; all roles then wind down, wait (bounded) for the
@@ -35,7 +41,7 @@
 #include "ic_common.cuh"
 #include "ic_kernels.h"
 #include "tc_utils.cuh"
-#include "topk_select.cuh"
+#include "topk_stream.cuh"
 
 namespace ic {
 namespace {
@@ -46,9 +52,10 @@ constexpr int DD = 128;                  // indexer feature dim
 constexpr int NCOL = QPB * HH;           // MMA N = 256
 constexpr int KT = 128;                  // keys per tile (MMA M)
 constexpr int KSTAGES = 4;               // ring of K-half tiles (16 KB each)
-constexpr int CAP = kMaxK + 512;         // candidate slots per row
+constexpr int CAP = kMaxK + 768;         // candidate slots per row
 constexpr int WG_THREADS = 128;
-constexpr int SEG = CAP / WG_THREADS;    // 20 entries per thread in a cut
+constexpr int SEG = CAP / WG_THREADS;    // entries per thread in a cut
+constexpr int CUT_LIMIT = CAP - 2 * KT;  // a cut leaves room for at least two tiles
 constexpr int NWARPS = 10;
 constexpr int NTHREADS = NWARPS * 32;
 constexpr uint32_t TMEM_COLS = 512;
@@ -58,7 +65,7 @@ struct __align__(1024) TcSmem {
   uint8_t qb[2][NCOL * 128];             // B operand: two K-halves, 256 rows x 128 B (SW128)
   uint8_t kst[KSTAGES][KT * 128];        // A operand ring: K-half tiles, 128 rows x 128 B (SW128)
   float wsm[QPB][HH];
-  float cand_s[QPB][CAP];
+  uint32_t cand_k[QPB][CAP];             // float_key of the score
   int cand_p[QPB][CAP];
   uint64_t full[KSTAGES];
   uint64_t empty[KSTAGES];
@@ -68,9 +75,10 @@ struct __align__(1024) TcSmem {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  int cnt[QPB];
-  uint32_t tau[QPB];
-  int wc[2][2][4];                       // [warpgroup][row][key quarter] insert counts
+  // per tile parity, row and key quarter: insert count, largest and smallest inserted key
+  int xc[2][QPB][4];
+  uint32_t xmax[2][QPB][4];
+  uint32_t xmin[2][QPB][4];
   SelectScratch scr[2];
 };
 
@@ -119,7 +127,6 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
     sm.abort = 0;
     tc::fence_mbar_init();
   }
-  if (tid < QPB) { sm.cnt[tid] = 0; sm.tau[tid] = 0u; }
   for (int i = tid; i < QPB * HH; i += NTHREADS) {
     const int qi = i / HH, h = i % HH;
     sm.wsm[qi][h] = qi < nq ? a.w[(static_cast<size_t>(b) * a.T + t0 + qi) * HH + h] : 0.0f;
@@ -200,16 +207,21 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
     const WgSync wsync{1 + wg};
     const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
     const int q0 = 2 * wg;
+    const unsigned lanes_below = (1u << lane) - 1u;
+    // per-row state, identical in every thread of the warpgroup
+    int cnt[2] = {0, 0};
+    uint32_t tau[2] = {0u, 0u};                     // a key enters iff key > tau
+    uint32_t rmin[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};  // bounds of the keys in the list
+    uint32_t rmax[2] = {0u, 0u};
 
     bool aborted = false;
     for (int j = 0; j < nt; ++j) {
       const int acc = j & 1;
-      bool ok = tc::mbar_wait(&sm.tfull[acc], (j >> 1) & 1, &sm.abort);
+      const int par = j & 1;
+      const bool ok = tc::mbar_wait(&sm.tfull[acc], (j >> 1) & 1, &sm.abort);
       if (!ok) set_abort(sm, status);
-      // one decision for the whole warpgroup
-      if (tc::named_sync_or(1 + wg, WG_THREADS, !ok || sm.abort)) { aborted = true; break; }
       tc::tc_fence_after();
-      float score[2];
+      uint32_t key[2];
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
         const uint32_t col = tmem + lane_field + acc * NCOL + (q0 + qq) * HH;
@@ -218,83 +230,95 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
         tc::tmem_ld_x32(col + 32, r1);
         tc::tmem_wait_ld();
         const float* wq = sm.wsm[q0 + qq];
-        float s = 0.0f;
+        float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;   // four chains: the FMA latencies overlap
 #pragma unroll
         for (int h = 0; h < 32; h += 4) {
           const float4 w4 = *reinterpret_cast<const float4*>(wq + h);
-          s = fmaf(w4.x, fmaxf(__uint_as_float(r0[h + 0]), 0.0f), s);
-          s = fmaf(w4.y, fmaxf(__uint_as_float(r0[h + 1]), 0.0f), s);
-          s = fmaf(w4.z, fmaxf(__uint_as_float(r0[h + 2]), 0.0f), s);
-          s = fmaf(w4.w, fmaxf(__uint_as_float(r0[h + 3]), 0.0f), s);
+          s0 = fmaf(w4.x, fmaxf(__uint_as_float(r0[h + 0]), 0.0f), s0);
+          s1 = fmaf(w4.y, fmaxf(__uint_as_float(r0[h + 1]), 0.0f), s1);
+          s2 = fmaf(w4.z, fmaxf(__uint_as_float(r0[h + 2]), 0.0f), s2);
+          s3 = fmaf(w4.w, fmaxf(__uint_as_float(r0[h + 3]), 0.0f), s3);
         }
 #pragma unroll
         for (int h = 0; h < 32; h += 4) {
           const float4 w4 = *reinterpret_cast<const float4*>(wq + 32 + h);
-          s = fmaf(w4.x, fmaxf(__uint_as_float(r1[h + 0]), 0.0f), s);
-          s = fmaf(w4.y, fmaxf(__uint_as_float(r1[h + 1]), 0.0f), s);
-          s = fmaf(w4.z, fmaxf(__uint_as_float(r1[h + 2]), 0.0f), s);
-          s = fmaf(w4.w, fmaxf(__uint_as_float(r1[h + 3]), 0.0f), s);
+          s0 = fmaf(w4.x, fmaxf(__uint_as_float(r1[h + 0]), 0.0f), s0);
+          s1 = fmaf(w4.y, fmaxf(__uint_as_float(r1[h + 1]), 0.0f), s1);
+          s2 = fmaf(w4.z, fmaxf(__uint_as_float(r1[h + 2]), 0.0f), s2);
+          s3 = fmaf(w4.w, fmaxf(__uint_as_float(r1[h + 3]), 0.0f), s3);
         }
-        score[qq] = s;
+        key[qq] = float_key((s0 + s1) + (s2 + s3));
       }
       tc::tc_fence_before();
       tc::mbar_arrive(&sm.tempty[acc]);           // accumulator may be overwritten
 
-      // cut back any list that could overflow during this tile
-#pragma unroll 1
-      for (int qq = 0; qq < 2; ++qq) {
-        const int qi = q0 + qq;
-        const int c = sm.cnt[qi];
-        if (qi < nq && c > CAP - KT) {
-          select_keep_topk<WG_THREADS, SEG>(sm.cand_s[qi], sm.cand_p[qi], c, a.k, &sm.scr[wg], wtid, wsync);
-          if (wtid == 0) { sm.cnt[qi] = a.k; sm.tau[qi] = sm.scr[wg].tau; }
-          wsync();
-        }
-      }
-      // ordered insertion of the keys above tau
+      // this warp's candidates of the tile; counts and key bounds go to the other warps
       const int s_pos = j * KT + key_local;
-      bool take[2];
+      bool valid[2], take[2];
       unsigned bal[2];
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
         const int qi = q0 + qq;
-        take[qq] = qi < nq && s_pos <= pos0 + qi && float_key(score[qq]) > sm.tau[qi];
+        valid[qq] = qi < nq && s_pos <= pos0 + qi;
+        take[qq] = valid[qq] && key[qq] > tau[qq];
         bal[qq] = __ballot_sync(0xffffffffu, take[qq]);
-        if (lane == 0) sm.wc[wg][qq][quarter] = __popc(bal[qq]);
+        const uint32_t mx = __reduce_max_sync(0xffffffffu, take[qq] ? key[qq] : 0u);
+        const uint32_t mn = __reduce_min_sync(0xffffffffu, take[qq] ? key[qq] : 0xFFFFFFFFu);
+        if (lane == 0) {
+          sm.xc[par][qi][quarter] = __popc(bal[qq]);
+          sm.xmax[par][qi][quarter] = mx;
+          sm.xmin[par][qi][quarter] = mn;
+        }
       }
-      wsync();
+      // the tile's one barrier: the exchange, and one abort decision for the warpgroup
+      if (tc::named_sync_or(1 + wg, WG_THREADS, !ok || sm.abort)) { aborted = true; break; }
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
         const int qi = q0 + qq;
+        int tot = sm.xc[par][qi][0] + sm.xc[par][qi][1] + sm.xc[par][qi][2] + sm.xc[par][qi][3];
+        if (cnt[qq] + tot > CAP) {
+          // the list would overflow: cut it, raise tau, recount this tile's keys
+          uint32_t thr;
+          cnt[qq] = cut_list<WG_THREADS, SEG>(sm.cand_k[qi], sm.cand_p[qi], cnt[qq], a.k, CUT_LIMIT, rmin[qq],
+                                              rmax[qq], &sm.scr[wg], wtid, wsync, &thr);
+          tau[qq] = thr;
+          rmin[qq] = thr;
+          take[qq] = valid[qq] && key[qq] > tau[qq];
+          bal[qq] = __ballot_sync(0xffffffffu, take[qq]);
+          if (lane == 0) sm.xc[par][qi][quarter] = __popc(bal[qq]);
+          wsync();
+          tot = sm.xc[par][qi][0] + sm.xc[par][qi][1] + sm.xc[par][qi][2] + sm.xc[par][qi][3];
+        }
+        if (tot == 0) continue;
+        int off = cnt[qq];
+        for (int x = 0; x < quarter; ++x) off += sm.xc[par][qi][x];
         if (take[qq]) {
-          int off = __popc(bal[qq] & ((1u << lane) - 1u));
-          for (int x = 0; x < quarter; ++x) off += sm.wc[wg][qq][x];
-          const int slot = sm.cnt[qi] + off;
-          sm.cand_s[qi][slot] = score[qq];
+          const int slot = off + __popc(bal[qq] & lanes_below);
+          sm.cand_k[qi][slot] = key[qq];
           sm.cand_p[qi][slot] = s_pos;
         }
-      }
-      wsync();
-      if (wtid < 2) {
-        const int qi = q0 + wtid;
-        sm.cnt[qi] += sm.wc[wg][wtid][0] + sm.wc[wg][wtid][1] + sm.wc[wg][wtid][2] + sm.wc[wg][wtid][3];
+        cnt[qq] += tot;
+        rmax[qq] = max(rmax[qq], max(max(sm.xmax[par][qi][0], sm.xmax[par][qi][1]),
+                                     max(sm.xmax[par][qi][2], sm.xmax[par][qi][3])));
+        rmin[qq] = min(rmin[qq], min(min(sm.xmin[par][qi][0], sm.xmin[par][qi][1]),
+                                     min(sm.xmin[par][qi][2], sm.xmin[par][qi][3])));
       }
     }
     if (!aborted) aborted = tc::named_sync_or(1 + wg, WG_THREADS, sm.abort != 0);
-    // final cut to k and write-out (ascending already)
+    // exact cut to k and write-out (ascending already)
     if (!aborted) {
-#pragma unroll 1
+#pragma unroll
       for (int qq = 0; qq < 2; ++qq) {
         const int qi = q0 + qq;
         if (qi >= nq) break;
-        const int c = sm.cnt[qi];
+        int c = cnt[qq];
         if (c > a.k) {
-          select_keep_topk<WG_THREADS, SEG>(sm.cand_s[qi], sm.cand_p[qi], c, a.k, &sm.scr[wg], wtid, wsync);
-          wsync();
+          uint32_t thr;
+          c = cut_list<WG_THREADS, SEG>(sm.cand_k[qi], sm.cand_p[qi], c, a.k, a.k, rmin[qq], rmax[qq], &sm.scr[wg],
+                                        wtid, wsync, &thr);
         }
-        const int n = min(c, a.k);
         int32_t* row = out + static_cast<size_t>(qi) * a.k;
-        for (int x = wtid; x < a.k; x += WG_THREADS) row[x] = x < n ? sm.cand_p[qi][x] : -1;
+        for (int x = wtid; x < a.k; x += WG_THREADS) row[x] = x < c ? sm.cand_p[qi][x] : -1;
       }
     }
   }

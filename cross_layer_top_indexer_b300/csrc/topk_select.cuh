@@ -4,8 +4,12 @@
 // position.  The 64-bit composite (float_key(score) << 32) | ~position is
 // therefore strictly larger for every preferred candidate, and all
 // composites are distinct.  Selection keeps the k largest composites with a
-// most-significant-digit radix select (8-bit digits), and compaction keeps
-// the survivors in their original (ascending position) order.
+// most-significant-digit radix select (up to 8-bit digits), and compaction
+// keeps the survivors in their original (ascending position) order.
+//
+// The caller passes bounds that every candidate satisfies (its score key
+// lies in [lo_key, hi_key], its position in [0, max_pos]); the leading bits
+// those bounds share are common to all candidates and are not histogrammed.
 #pragma once
 #include "ic_common.cuh"
 
@@ -56,28 +60,36 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int n
   return r;
 }
 
+// Mask of the top `bits` bits of a word (0 <= bits <= 32).
+__device__ __forceinline__ uint32_t top_mask(int bits) { return bits <= 0 ? 0u : (0xFFFFFFFFu << (32 - bits)); }
+
 // Keep the k best of the n candidates (sc[0..n), pos[0..n)), in place and in
 // order; returns through scr->tau the smallest kept float_key.  n > k >= 1.
-// All threads of the block must call it.  SEG = max entries per thread.
+// All threads of the group must call it.  SEG = max entries per thread
+// (n <= NTHREADS * SEG).  Bounds: lo_key <= float_key(sc[i]) <= hi_key and
+// 0 <= pos[i] <= max_pos for every i.
 template <int NTHREADS, int SEG, class Sync = BlockSync>
-__device__ void select_keep_topk(float* sc, int* pos, int n, int k, SelectScratch* scr, int tid = -1,
-                                 Sync sync = Sync()) {
-  if (tid < 0) tid = threadIdx.x;
+__device__ void select_keep_topk(float* sc, int* pos, int n, int k, SelectScratch* scr, int tid, Sync sync,
+                                 uint32_t lo_key, uint32_t hi_key, uint32_t max_pos) {
   const int lane = tid & 31, wid = tid >> 5;
-  uint32_t pre_hi = 0, msk_hi = 0, pre_lo = 0, msk_lo = 0;
+  // bits shared by every candidate: the common prefix of the bounds
+  int kh = lo_key == hi_key ? 32 : __clz(lo_key ^ hi_key);
+  int kl = max_pos == 0 ? 32 : __clz(max_pos);     // ~pos lies in [~max_pos, 0xFFFFFFFF]
+  uint32_t msk_hi = top_mask(kh), pre_hi = hi_key & msk_hi;
+  uint32_t msk_lo = top_mask(kl), pre_lo = 0xFFFFFFFFu & msk_lo;
   int need = k;
-  for (int pass = 0; pass < 8; ++pass) {
-    const bool hi_word = pass < 4;
-    const int shift = 24 - 8 * (pass & 3);
+  while (kh < 32 || kl < 32) {
+    const bool hw = kh < 32;
+    const int known = hw ? kh : kl;
+    const int w = min(8, 32 - known);
+    const int shift = 32 - known - w;
+    const uint32_t dmask = (1u << w) - 1u;
     for (int i = tid; i < 256; i += NTHREADS) scr->hist[i] = 0;
     sync();
     for (int i = tid; i < n; i += NTHREADS) {
-      uint32_t h = float_key(sc[i]);
-      uint32_t l = ~(uint32_t)pos[i];
-      if ((h & msk_hi) == pre_hi && (l & msk_lo) == pre_lo) {
-        uint32_t d = ((hi_word ? h : l) >> shift) & 255u;
-        atomicAdd(&scr->hist[d], 1);
-      }
+      const uint32_t h = float_key(sc[i]);
+      const uint32_t l = ~static_cast<uint32_t>(pos[i]);
+      if ((h & msk_hi) == pre_hi && (l & msk_lo) == pre_lo) atomicAdd(&scr->hist[((hw ? h : l) >> shift) & dmask], 1);
     }
     sync();
     if (wid == 0) {
@@ -107,47 +119,59 @@ __device__ void select_keep_topk(float* sc, int* pos, int n, int k, SelectScratc
       }
     }
     sync();
-    const uint32_t dsel = (uint32_t)scr->sel_digit;
+    const uint32_t dsel = static_cast<uint32_t>(scr->sel_digit);
     need = scr->sel_need;
     const int done = scr->sel_done;
-    if (hi_word) { pre_hi |= dsel << shift; msk_hi |= 255u << shift; }
-    else         { pre_lo |= dsel << shift; msk_lo |= 255u << shift; }
+    if (hw) { pre_hi |= dsel << shift; msk_hi |= dmask << shift; kh += w; }
+    else    { pre_lo |= dsel << shift; msk_lo |= dmask << shift; kl += w; }
     sync();
     if (done) break;
   }
-  // Ordered compaction: contiguous segment per thread, block scan of counts.
+  // Ordered compaction in two halves (fewer registers): contiguous segment
+  // per thread, block scan of the counts.  Every write lands at or below the
+  // index it came from, and each half is read into registers before any of
+  // its writes.
   if (tid == 0) scr->tau = 0xffffffffu;
-  float vs[SEG];
-  int vp[SEG];
-  int keep = 0;
-  unsigned flags = 0;
-  const int seg = (n + NTHREADS - 1) / NTHREADS;
-  const int b0 = tid * seg;
-#pragma unroll
-  for (int j = 0; j < SEG; ++j) {
-    const int i = b0 + j;
-    if (j < seg && i < n) {
-      vs[j] = sc[i];
-      vp[j] = pos[i];
-      uint32_t h = float_key(vs[j]);
-      uint32_t l = ~(uint32_t)vp[j];
-      uint32_t mh = h & msk_hi, ml = l & msk_lo;
-      bool take = (mh > pre_hi) || (mh == pre_hi && ml >= pre_lo);
-      if (take) { flags |= 1u << j; ++keep; }
-    }
-  }
-  int total;
-  int off = block_exclusive_scan(keep, scr->warp_sums, NTHREADS, total, tid, sync);
   uint32_t local_min = 0xffffffffu;
+  constexpr int HS = (SEG + 1) / 2;
+  int written = 0;
+  const int half_n = (n + 1) / 2;
+#pragma unroll 1
+  for (int part = 0; part < 2; ++part) {
+    const int p0 = part ? half_n : 0;
+    const int pn = part ? n - half_n : half_n;
+    float vs[HS];
+    int vp[HS];
+    int keep = 0;
+    unsigned flags = 0;
+    const int seg = (pn + NTHREADS - 1) / NTHREADS;
+    const int b0 = p0 + tid * seg;
 #pragma unroll
-  for (int j = 0; j < SEG; ++j) {
-    if (flags & (1u << j)) {
-      sc[off] = vs[j];
-      pos[off] = vp[j];
-      ++off;
-      uint32_t h = float_key(vs[j]);
-      local_min = h < local_min ? h : local_min;
+    for (int j = 0; j < HS; ++j) {
+      const int i = b0 + j;
+      if (j < seg && i < p0 + pn) {
+        vs[j] = sc[i];
+        vp[j] = pos[i];
+        const uint32_t mh = float_key(vs[j]) & msk_hi;
+        const uint32_t ml = ~static_cast<uint32_t>(vp[j]) & msk_lo;
+        const bool take = (mh > pre_hi) || (mh == pre_hi && ml >= pre_lo);
+        if (take) { flags |= 1u << j; ++keep; }
+      }
     }
+    int total;
+    int off = written + block_exclusive_scan(keep, scr->warp_sums, NTHREADS, total, tid, sync);
+#pragma unroll
+    for (int j = 0; j < HS; ++j) {
+      if (flags & (1u << j)) {
+        sc[off] = vs[j];
+        pos[off] = vp[j];
+        ++off;
+        const uint32_t h = float_key(vs[j]);
+        local_min = h < local_min ? h : local_min;
+      }
+    }
+    written += total;
+    sync();
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
