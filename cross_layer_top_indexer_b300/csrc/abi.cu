@@ -112,6 +112,7 @@ ic_status run_indexer(const ic::IndexerArgs& a, void* ws, size_t ws_bytes, cudaS
     const size_t need = ic::indexer_decode_ws_bytes(a.B, a.T, a.S);
     if (ws_bytes < need || (need && !ws))
       return fail(IC_ERR_ARG, "workspace of %zu bytes is smaller than the %zu needed", ws_bytes, need);
+    if (need && !aligned16(ws)) return fail(IC_ERR_ARG, "workspace must be 16-byte aligned");
     e = ic::launch_indexer_decode(a, ws, ws_bytes, status, st);
   } else if (ic::indexer_prefill_tc_supported(a)) {
     e = ic::launch_indexer_prefill_tc(a, status, st);
@@ -125,6 +126,7 @@ ic_status run_attn(const ic::AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_
   const size_t need = ic::attn_ws_bytes(a.B, a.T, a.Hq, a.Dh, a.k);
   if (ws_bytes < need || (need && !ws))
     return fail(IC_ERR_ARG, "workspace of %zu bytes is smaller than the %zu needed", ws_bytes, need);
+  if (need && !aligned16(ws)) return fail(IC_ERR_ARG, "workspace must be 16-byte aligned");
   cudaError_t e = ic::launch_sparse_attn(a, ws, ws_bytes, device_status_ptr(), st);
   return e == cudaSuccess ? IC_OK : cuda_fail(e, "sparse attention launch");
 }

@@ -44,6 +44,10 @@ cudaError_t launch_indexer_decode(const IndexerArgs& a, void* ws, size_t ws_byte
                                   cudaStream_t st);
 // Rows per sequence at or below which the indexer takes the decode path.
 constexpr int kDecodeMaxT = 8;
+// Tensor-core decode scores for one query row per sequence, H = 64, D = 128:
+bool indexer_decode_tc_supported(const IndexerArgs& a);
+cudaError_t launch_indexer_decode_tc(const IndexerArgs& a, float* scores, size_t pitch, int* dev_status,
+                                     cudaStream_t st);
 
 // Sparse attention; splits the k rows over CTAs (partials in ws) when few rows.
 size_t attn_ws_bytes(int B, int T, int Hq, int Dh, int k);

@@ -5,11 +5,11 @@
 // but the work is spread over the KEYS: one CTA per (tile of keys, query
 // row), so a handful of query rows still fills the GPU.  Each query row's
 // causal scores are staged in the workspace (one fp32 row per query, O(L),
-// never an L x L matrix), then one CTA per row selects the exact top-k with
-// a most-significant-digit radix select and writes the positions in
-// ascending order.
+// never an L x L matrix), then one CTA per row selects the exact top-k and
+// writes the positions in ascending order.
 #include "ic_common.cuh"
 #include "ic_kernels.h"
+#include "topk_stream.cuh"
 
 namespace ic {
 namespace {
@@ -145,26 +145,18 @@ decode_scores_kernel(IndexerArgs a, float* scores, int h_pad, size_t pitch) {
 // Exact top-k of one staged score row (one CTA per row).
 // ---------------------------------------------------------------------------
 
-constexpr int STHREADS = 1024;
+constexpr int STHREADS = 512;
 constexpr int SWARPS = STHREADS / 32;
 
-__global__ void __launch_bounds__(STHREADS)
-decode_select_kernel(const float* scores, size_t pitch, int32_t* idx, int T, int q_pos0, int k) {
+// General path: most-significant-digit radix select over the composite
+// (score key, ~position), one pass over the row per 8-bit digit, then an
+// ordered write.  Used when the fast path's candidate set does not fit.
+__device__ void radix_select_row(const float* sc, int n, int k, int32_t* out) {
   __shared__ int whist[SWARPS][256];
   __shared__ int hist[256];
   __shared__ int wsum[33];
   __shared__ int sel_digit, sel_need, sel_done;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int row = blockIdx.x;
-  const int t = row % T;
-  const int n = q_pos0 + t + 1;
-  const float* sc = scores + (size_t)row * pitch;
-  int32_t* out = idx + (size_t)row * k;
-
-  if (n <= k) {
-    for (int j = tid; j < k; j += STHREADS) out[j] = j < n ? j : -1;
-    return;
-  }
   uint32_t pre_hi = 0, msk_hi = 0, pre_lo = 0, msk_lo = 0;
   int need = k;
   for (int pass = 0; pass < 8; ++pass) {
@@ -243,7 +235,7 @@ decode_select_kernel(const float* scores, size_t pitch, int32_t* idx, int T, int
     if (lane == 31) wsum[wid] = incl;
     __syncthreads();
     if (wid == 0) {
-      const int s = wsum[lane];
+      const int s = lane < SWARPS ? wsum[lane] : 0;
       int si = s;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -266,6 +258,164 @@ decode_select_kernel(const float* scores, size_t pitch, int32_t* idx, int T, int
   }
 }
 
+// Fast path.  Pass 1 histograms the top 12 bits of every score key; the bin
+// holding the k-th largest key is the threshold bin.  Pass 2 copies, in
+// position order, every entry whose key is in or above that bin into shared
+// memory (each warp takes a contiguous segment: it counts its entries, the
+// warps' offsets are scanned, and a second sweep writes them with warp
+// prefix sums).  If more than k were copied, cut_list keeps exactly the k
+// best, ties to the earlier (lower) position.  The row is read three times,
+// from L2, where the scoring kernel just wrote it.
+constexpr int FBITS = 12;
+constexpr int FBINS = 1 << FBITS;
+constexpr int FSEG = 16;
+constexpr int FCAP = STHREADS * FSEG;    // candidates held in shared memory
+
+struct FastSelSmem {
+  int hist[FBINS];
+  uint32_t key[FCAP];
+  int pos[FCAP];
+  int woff[SWARPS];
+  SelectScratch scr;
+  int bsel, ncand;
+};
+
+__device__ __forceinline__ float4 load_row4(const float* sc, int i, int n) {
+  if (i + 3 < n) return __ldcg(reinterpret_cast<const float4*>(sc + i));
+  float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (i < n) v.x = sc[i];
+  if (i + 1 < n) v.y = sc[i + 1];
+  if (i + 2 < n) v.z = sc[i + 2];
+  return v;
+}
+
+__global__ void __launch_bounds__(STHREADS)
+decode_select_kernel(const float* scores, size_t pitch, int32_t* idx, int T, int q_pos0, int k) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  FastSelSmem& sm = *reinterpret_cast<FastSelSmem*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int row = blockIdx.x;
+  const int t = row % T;
+  const int n = q_pos0 + t + 1;
+  const float* sc = scores + (size_t)row * pitch;    // 16-byte aligned rows
+  int32_t* out = idx + (size_t)row * k;
+
+  if (n <= k) {
+    for (int j = tid; j < k; j += STHREADS) out[j] = j < n ? j : -1;
+    return;
+  }
+  // ---- pass 1: histogram of key >> 20
+  for (int i = tid; i < FBINS; i += STHREADS) sm.hist[i] = 0;
+  __syncthreads();
+  constexpr int UNR = 8;
+  for (int base = 4 * tid; base < n; base += 4 * STHREADS * UNR) {
+    float4 v[UNR];
+#pragma unroll
+    for (int j = 0; j < UNR; ++j) v[j] = load_row4(sc, base + 4 * STHREADS * j, n);
+#pragma unroll
+    for (int j = 0; j < UNR; ++j) {
+      const int i = base + 4 * STHREADS * j;
+      if (i < n) atomicAdd(&sm.hist[float_key(v[j].x) >> 20], 1);
+      if (i + 1 < n) atomicAdd(&sm.hist[float_key(v[j].y) >> 20], 1);
+      if (i + 2 < n) atomicAdd(&sm.hist[float_key(v[j].z) >> 20], 1);
+      if (i + 3 < n) atomicAdd(&sm.hist[float_key(v[j].w) >> 20], 1);
+    }
+  }
+  __syncthreads();
+  // ---- threshold bin: thread t holds bins FBINS-1-8t .. FBINS-8-8t (descending)
+  {
+    constexpr int BPT = FBINS / STHREADS;
+    int c[BPT];
+    int s = 0;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) { c[j] = sm.hist[FBINS - 1 - BPT * tid - j]; s += c[j]; }
+    int total;
+    const int excl = block_exclusive_scan(s, sm.scr.warp_sums, STHREADS, total, tid, BlockSync());
+    if (excl < k && k <= excl + s) {
+      int cum = excl;
+#pragma unroll
+      for (int j = 0; j < BPT; ++j) {
+        if (cum + c[j] >= k) { sm.bsel = FBINS - 1 - BPT * tid - j; sm.ncand = cum + c[j]; break; }
+        cum += c[j];
+      }
+    }
+  }
+  __syncthreads();
+  const int ncand = sm.ncand;
+  if (ncand > FCAP) {
+    radix_select_row(sc, n, k, out);
+    return;
+  }
+  const uint32_t lo = static_cast<uint32_t>(sm.bsel) << 20;
+  // ---- pass 2: ordered copy of the keys >= lo; warp wid takes [seg0, seg1)
+  const int segE = ((n + SWARPS - 1) / SWARPS + 127) & ~127;
+  const int seg0 = min(n, wid * segE), seg1 = min(n, seg0 + segE);
+  int cnt = 0;
+  for (int c0 = seg0; c0 < seg1; c0 += 128 * 4) {
+    float4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = load_row4(sc, c0 + 128 * j + 4 * lane, seg1);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = c0 + 128 * j + 4 * lane;
+      cnt += (i < seg1 && float_key(v[j].x) >= lo) + (i + 1 < seg1 && float_key(v[j].y) >= lo) +
+             (i + 2 < seg1 && float_key(v[j].z) >= lo) + (i + 3 < seg1 && float_key(v[j].w) >= lo);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if (lane == 0) sm.woff[wid] = cnt;
+  __syncthreads();
+  if (wid == 0) {
+    const int v = lane < SWARPS ? sm.woff[lane] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    if (lane < SWARPS) sm.woff[lane] = incl - v;
+  }
+  __syncthreads();
+  int off = sm.woff[wid];
+  for (int c0 = seg0; c0 < seg1; c0 += 128) {
+    const int i = c0 + 4 * lane;
+    const float4 v = load_row4(sc, i, seg1);
+    const uint32_t kk[4] = {float_key(v.x), float_key(v.y), float_key(v.z), float_key(v.w)};
+    unsigned f = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (i + j < seg1 && kk[j] >= lo) f |= 1u << j;
+    const int c = __popc(f);
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += u;
+    }
+    int o2 = off + incl - c;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (f & (1u << j)) { sm.key[o2] = kk[j]; sm.pos[o2] = i + j; ++o2; }
+    off += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  __syncthreads();
+  if (ncand > k) {
+    uint32_t thr;
+    cut_list<STHREADS, FSEG>(sm.key, sm.pos, ncand, k, k, lo, 0xFFFFFFFFu, &sm.scr, tid, BlockSync(), &thr);
+  }
+  for (int j = tid; j < k; j += STHREADS) out[j] = sm.pos[j];
+}
+
+cudaError_t launch_select(float* scores, size_t pitch, const IndexerArgs& a, cudaStream_t st) {
+  const size_t smem = sizeof(FastSelSmem);
+  cudaError_t e = cudaFuncSetAttribute(decode_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  decode_select_kernel<<<a.B * a.T, STHREADS, smem, st>>>(scores, pitch, a.idx, a.T, a.q_pos0, a.k);
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_scores(const IndexerArgs& a, float* scores, size_t pitch, cudaStream_t st) {
   const int h_pad = ((a.H + 15) / 16) * 16;
@@ -283,12 +433,17 @@ cudaError_t launch_scores(const IndexerArgs& a, float* scores, size_t pitch, cud
 
 size_t indexer_decode_ws_bytes(int B, int T, int S) { return (size_t)B * T * row_pitch(S) * sizeof(float); }
 
-cudaError_t launch_indexer_decode(const IndexerArgs& a, void* ws, size_t ws_bytes, int* /*dev_status*/,
+cudaError_t launch_indexer_decode(const IndexerArgs& a, void* ws, size_t ws_bytes, int* dev_status,
                                   cudaStream_t st) {
   if (ws_bytes < indexer_decode_ws_bytes(a.B, a.T, a.S)) return cudaErrorInvalidValue;
   float* scores = reinterpret_cast<float*>(ws);
   const size_t pitch = row_pitch(a.S);
   cudaError_t e;
+  if (indexer_decode_tc_supported(a)) {
+    e = launch_indexer_decode_tc(a, scores, pitch, dev_status, st);
+    if (e != cudaSuccess) return e;
+    return launch_select(scores, pitch, a, st);
+  }
   switch (a.D) {
     case 32: e = launch_scores<32>(a, scores, pitch, st); break;
     case 64: e = launch_scores<64>(a, scores, pitch, st); break;
@@ -296,8 +451,7 @@ cudaError_t launch_indexer_decode(const IndexerArgs& a, void* ws, size_t ws_byte
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  decode_select_kernel<<<a.B * a.T, STHREADS, 0, st>>>(scores, pitch, a.idx, a.T, a.q_pos0, a.k);
-  return cudaGetLastError();
+  return launch_select(scores, pitch, a, st);
 }
 
 }  // namespace ic

@@ -91,7 +91,9 @@ typedef struct ic_layer {
 
 /* Bytes of device workspace the calls below need for these sizes (the
  * maximum over ic_indexer_topk, ic_sparse_attn and ic_forward_pattern).
- * Returns 0 for sizes that need none; (size_t)-1 for invalid dims. */
+ * Returns 0 for sizes that need none; (size_t)-1 for invalid dims.  A
+ * workspace passed to those calls is caller-owned device memory, 16-byte
+ * aligned (IC_ERR_ARG otherwise). */
 size_t ic_workspace_size(const ic_dims* dims);
 
 /* Lightning indexer + top-k, one Full layer

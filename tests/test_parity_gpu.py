@@ -205,6 +205,61 @@ def test_indexer_decode_path(Bn, T, S, S_cap, q_pos0, k, kd):
     pu.check_recall(stats)
 
 
+@pytest.mark.parametrize("Bn,S,k,mode", [(3, 1300, 256, "codes"), (2, 777, 100, "int"), (5, 4099, 2048, "codes")])
+def test_decode_e4m3_every_code(Bn, S, k, mode):
+    # decode keys drawn from every e4m3 code but NaN (zeros, subnormals, the
+    # largest magnitudes) exercise the exact widening to bf16 in the kernel
+    g = torch.Generator(device="cpu").manual_seed(17)
+    codes = torch.tensor([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=torch.uint8)
+    kb = codes[torch.randint(0, len(codes), (Bn, S, 128), generator=g)]
+    if mode == "int":
+        # small integers: exact products, bit-exact selection
+        ints = torch.tensor([0x00, 0x38, 0x40, 0x44, 0xB8, 0xC0, 0xC4], dtype=torch.uint8)   # 0, 1, 2, 3, -1, -2, -3
+        kb = ints[torch.randint(0, len(ints), (Bn, S, 128), generator=g)]
+        q = torch.randint(-2, 3, (Bn, 1, 64, 128), generator=g).float()
+        w = torch.randint(-2, 3, (Bn, 1, 64), generator=g).float()
+        ks = torch.ones(Bn, S)
+    else:
+        q = torch.randn(Bn, 1, 64, 128, generator=g) / 11.3
+        w = torch.randn(Bn, 1, 64, generator=g) / 8
+        ks = torch.rand(Bn, S, generator=g) * 0.01 + 1e-3
+    kI = kb.view(torch.float8_e4m3fn).to(DEV)
+    q, w, ks = q.to(DEV, torch.bfloat16), w.to(DEV), ks.to(DEV)
+    idx = B.indexer_topk(q, kI, w, k, S - 1, kscale=ks, S=S)
+    torch.cuda.synchronize()
+    got = _idx64(idx)
+    stats = {"hit": 0, "tot": 0}
+    for b in range(Bn):
+        pu.check_topk(got[b], pu.to_f64(q[b]), pu.keys_f64(kI[b], ks[b]), pu.to_f64(w[b]), k, S - 1, [0],
+                      exact=(mode == "int"), stats=stats)
+    if mode != "int":
+        pu.check_recall(stats)
+
+
+@pytest.mark.parametrize("S,n_top,top_val", [
+    (20000, 0, 0.0),        # every score equal: the threshold bin holds the whole row
+    (6000, 2500, 1.0),      # more tied top scores than k, all within the candidate buffer
+    (30000, 9000, 2.0),     # more tied top scores than the candidate buffer holds
+])
+def test_decode_select_ties(S, n_top, top_val):
+    # score = ReLU(kI[s, 0]) through head 0 only; ties go to the lower positions
+    k, Bn = 2048, 2
+    g = torch.Generator(device="cpu").manual_seed(S)
+    q = torch.zeros(Bn, 1, 64, 128)
+    q[:, 0, 0, 0] = 1.0
+    kI = torch.zeros(Bn, S, 128)
+    for b in range(Bn):
+        kI[b, torch.randperm(S, generator=g)[:n_top], 0] = top_val
+        kI[b, torch.randperm(S, generator=g)[:S // 3], 1] = 0.5     # head 0 ignores feature 1
+    w = torch.zeros(Bn, 1, 64)
+    w[:, 0, 0] = 1.0
+    q, kI, w = q.to(DEV, torch.bfloat16), kI.to(DEV, torch.bfloat16), w.to(DEV)
+    got = _idx64(B.indexer_topk(q, kI, w, k, S - 1, S=S))
+    torch.cuda.synchronize()
+    for b in range(Bn):
+        pu.check_topk(got[b], pu.to_f64(q[b]), pu.to_f64(kI[b]), pu.to_f64(w[b]), k, S - 1, [0], exact=True)
+
+
 def test_decode_matches_prefill_row():
     # the decode kernels at position p give the prefill kernel's row p
     cfg = synth.StackConfig("x", 1, "F", 1, 1200, 1200, 64, 128, 128, 32, 128)
