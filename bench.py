@@ -289,10 +289,25 @@ def run_decode(binding, pattern, steps_tok, seed, dev, gpu_index):
     tr.close()
     del layers, fwds, ws
     torch.cuda.empty_cache()
+    idx_layer_ms = sum(idx_ms) / max(1, pattern.count("F"))
+    attn_layer_ms = sum(attn_ms) / len(pattern)
+    # algorithmic HBM bytes of one layer at the traced context S = S_cap:
+    # indexer: every cached key once (d_I e4m3 bytes + its fp32 scale) plus q, w
+    # and the index row; attention: the k selected K and V rows (bf16) plus Q, O
+    S = S_cap
+    idx_bytes = cfg.B * (S * (cfg.D + 4) + cfg.H * cfg.D * 2 + cfg.H * 4 + cfg.k * 4)
+    attn_bytes = cfg.B * (cfg.k * 2 * cfg.Dh * 2 + 2 * cfg.Hq * cfg.Dh * 2 + cfg.k * 4)
+    hbm = load_peaks()["hbm_gbs"]
+    roof = {}
+    for name, nbytes, t_ms in (("indexer_topk", idx_bytes, idx_layer_ms), ("sparse_attn", attn_bytes, attn_layer_ms)):
+        if t_ms > 0:
+            ach = nbytes / (t_ms * 1e-3) / 1e9
+            roof[name] = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+                          "bytes_per_launch": nbytes, "launch_ms": t_ms}
     return {"value": cfg.B * steps_tok / (ms * 1e-3), "unit": "tok/s", "ms_per_token_step": ms / steps_tok,
             "steps": steps_tok, "batch": cfg.B, "context": cfg.q_pos0, "pattern": pattern,
-            "indexer_ms_per_F_layer": sum(idx_ms) / max(1, pattern.count("F")),
-            "attn_ms_per_layer": sum(attn_ms) / len(pattern), "clocks": clk.summary()}
+            "indexer_ms_per_F_layer": idx_layer_ms, "attn_ms_per_layer": attn_layer_ms,
+            "kernels": roof, "clocks": clk.summary()}
 
 
 # ---------------------------------------------------------------------------

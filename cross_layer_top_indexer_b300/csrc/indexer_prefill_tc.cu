@@ -1,6 +1,6 @@
 // Fused lightning indexer + streaming top-k on the 5th-generation tensor
 // cores (tcgen05 + TMA + tensor memory), for the production indexer shape
-// H_I = 64 heads, d_I = 128, bf16 keys.
+// H_I = 64 heads, d_I = 128, bf16 keys or e4m3 keys with a per-key scale.
 //
 // Score (DSA lightning-indexer score, the Full layers of IndexCache; notes
 // page "NLP--IndexCache", section "背景 & 问题提出"):
@@ -13,13 +13,24 @@
 // the MMAs into two TMEM accumulators of 128 x 256 fp32 (all 512 columns),
 // so the tensor core fills one while the epilogue drains the other.
 //
-// Warp roles (10 warps):
-//   warp 0     TMA producer (q once, then key half-tiles)
+// Warp roles (10 warps; 12 for e4m3 keys):
+//   warp 0     TMA producer (q once, then key half-tiles; for e4m3 keys only q)
 //   warp 1     TMEM allocator + MMA issuer
 //   warps 2-9  epilogue: two warpgroups; warpgroup g owns query rows 2g and
 //              2g+1.  Thread = one key (its TMEM lane); it reads the 64 head
 //              dot products of each of its two rows, forms the weighted ReLU
 //              sum in registers, and runs the streaming top-k.
+//   warps 10-11 (e4m3 keys) widen each key tile from global memory into the
+//              ring as f16, exactly (every e4m3 value is an f16), with the
+//              hardware conversion.
+//
+// e4m3 keys: the MMA runs on f16 operands (kind::f16).  Each bf16 q row is
+// rewritten in place as f16 times a power of two 2^e_h that brings its
+// largest magnitude into [2^14, 2^15); f16 has 11 significant bits against
+// bf16's 8, so every element not below 2^-17 after scaling (a relative
+// 2^-31 of the row's largest) is carried exactly.  The weight w_h is
+// multiplied by 2^-e_h, so the epilogue is unchanged, and the key's scale
+// multiplies the score (a positive factor commutes with ReLU).
 //
 // Streaming top-k (per row, in shared memory): a candidate list of (key,
 // position), key = an order-preserving integer image of the score, kept in
@@ -56,10 +67,14 @@ constexpr int CAP = kMaxK + 768;         // candidate slots per row
 constexpr int WG_THREADS = 128;
 constexpr int SEG = CAP / WG_THREADS;    // entries per thread in a cut
 constexpr int CUT_LIMIT = CAP - 2 * KT;  // a cut leaves room for at least two tiles
-constexpr int NWARPS = 10;
+constexpr int NWARPS = 10;               // bf16 keys
 constexpr int NTHREADS = NWARPS * 32;
+constexpr int CONV_THREADS = 64;         // e4m3 keys: two more warps
+constexpr int NTHREADS_E4M3 = NTHREADS + CONV_THREADS;
+constexpr int EPI_THREADS = 8 * 32;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = tc::idesc_bf16_f32(KT, NCOL);
+constexpr uint32_t IDESC_F16 = tc::idesc_f16_f32(KT, NCOL);
 
 struct __align__(1024) TcSmem {
   uint8_t qb[2][NCOL * 128];             // B operand: two K-halves, 256 rows x 128 B (SW128)
@@ -72,6 +87,7 @@ struct __align__(1024) TcSmem {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t qfull;
+  uint64_t qconv;                        // e4m3 keys: q rewritten as scaled f16
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -92,7 +108,32 @@ __device__ __forceinline__ void set_abort(TcSmem& sm, int* status) {
   if (status) atomicExch(status, kDevTimeout);
 }
 
-__global__ void __launch_bounds__(NTHREADS, 1)
+// Eight bf16 (one 16-byte chunk) -> eight floats.
+__device__ __forceinline__ void bf16x8_to_f32(const uint4& c, float* f) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    f[2 * j] = __uint_as_float(w[j] << 16);
+    f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+  }
+}
+
+// Two e4m3 bytes (the low 16 bits, low byte first) -> two f16, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(v)));
+  return h2;
+}
+
+// Two floats -> packed f16x2 (round to nearest), `lo` in the low half.
+__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <bool E4M3>
+__global__ void __launch_bounds__(E4M3 ? NTHREADS_E4M3 : NTHREADS, 1)
 indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           IndexerArgs a, int n_groups, int* status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -109,8 +150,9 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
   const int n_keys = pos0 + nq;
   int32_t* out = a.idx + (static_cast<size_t>(b) * a.T + t0) * a.k;
 
+  constexpr int kThreads = E4M3 ? NTHREADS_E4M3 : NTHREADS;
   if (n_keys <= a.k) {   // every causal position of every row is selected
-    for (int i = tid; i < nq * a.k; i += NTHREADS) {
+    for (int i = tid; i < nq * a.k; i += kThreads) {
       const int qi = i / a.k, j = i - qi * a.k;
       out[i] = (j <= pos0 + qi) ? j : -1;
     }
@@ -120,14 +162,18 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
 
   // ---- set-up ----
   if (tid == 0) {
-    for (int s = 0; s < KSTAGES; ++s) { tc::mbar_init(&sm.full[s], 1); tc::mbar_init(&sm.empty[s], 1); }
-    for (int s = 0; s < 2; ++s) { tc::mbar_init(&sm.tfull[s], 1); tc::mbar_init(&sm.tempty[s], 8 * 32); }
+    for (int s = 0; s < KSTAGES; ++s) {
+      tc::mbar_init(&sm.full[s], E4M3 ? CONV_THREADS : 1);
+      tc::mbar_init(&sm.empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) { tc::mbar_init(&sm.tfull[s], 1); tc::mbar_init(&sm.tempty[s], EPI_THREADS); }
     tc::mbar_init(&sm.qfull, 1);
+    tc::mbar_init(&sm.qconv, EPI_THREADS);
     tc::mbar_init(&sm.drain, 1);
     sm.abort = 0;
     tc::fence_mbar_init();
   }
-  for (int i = tid; i < QPB * HH; i += NTHREADS) {
+  for (int i = tid; i < QPB * HH; i += kThreads) {
     const int qi = i / HH, h = i % HH;
     sm.wsm[qi][h] = qi < nq ? a.w[(static_cast<size_t>(b) * a.T + t0 + qi) * HH + h] : 0.0f;
   }
@@ -151,7 +197,7 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
       tc::tma_load_2d(sm.qb[1], &tm_q, &sm.qfull, 64, qrow);
       const int krow0 = b * a.S_cap;
       int issued = 0;
-      for (int it = 0; it < 2 * nt; ++it) {
+      for (int it = 0; !E4M3 && it < 2 * nt; ++it) {
         const int s = it % KSTAGES;
         const uint32_t ph = (it / KSTAGES) & 1;
         if (!tc::mbar_wait(&sm.empty[s], ph ^ 1, &sm.abort)) { set_abort(sm, status); break; }
@@ -168,7 +214,7 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
   } else if (warp == 1) {
     // ================= MMA issuer =================
     if (lane == 0) {
-      bool ok = tc::mbar_wait(&sm.qfull, 0, &sm.abort);
+      bool ok = tc::mbar_wait(E4M3 ? &sm.qconv : &sm.qfull, 0, &sm.abort);
       if (!ok) set_abort(sm, status);
       const uint32_t qb0 = tc::smem_u32(sm.qb[0]);
       const uint32_t qb1 = tc::smem_u32(sm.qb[1]);
@@ -186,8 +232,8 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
           const uint32_t b_base = h ? qb1 : qb0;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc::mma_f16(d_tmem, tc::sdesc_k_sw128(a_base + kk * 32), tc::sdesc_k_sw128(b_base + kk * 32), IDESC,
-                        (h | kk) != 0);
+            tc::mma_f16(d_tmem, tc::sdesc_k_sw128(a_base + kk * 32), tc::sdesc_k_sw128(b_base + kk * 32),
+                        E4M3 ? IDESC_F16 : IDESC, (h | kk) != 0);
           tc::mma_commit(&sm.empty[s]);   // frees the stage once these MMAs are done
         }
         if (!ok) break;
@@ -198,6 +244,62 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
       if (!tc::mbar_wait(&sm.drain, 0, nullptr, 4000000000ull)) set_abort(sm, status);
     }
     __syncwarp();
+  } else if (warp >= NWARPS) {
+    // ================= e4m3 keys -> f16 operand tiles =================
+    if constexpr (E4M3) {
+      const int ct = tid - NTHREADS;                // 0..63
+      const uint8_t* kbase = static_cast<const uint8_t*>(a.kI);
+      const long long krow0 = static_cast<long long>(b) * a.S_cap;
+      const long long nrows = static_cast<long long>(a.B) * a.S_cap;
+      // a tile is 128 rows x 128 B = 1024 pieces of 16 B; piece c = ct + 64u:
+      // row c >> 3, features 16 (c & 7) .. +15 (a warp reads 4 whole rows)
+      auto load_tile = [&](int j, uint4 (&raw)[16]) {
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int c = ct + 64 * u;
+          const long long row = krow0 + static_cast<long long>(j) * KT + (c >> 3);
+          raw[u] = row < nrows ? __ldg(reinterpret_cast<const uint4*>(kbase + row * DD + 16 * (c & 7)))
+                               : make_uint4(0u, 0u, 0u, 0u);
+        }
+      };
+      // both K-halves of tile j go to ring stages 2j, 2j+1
+      auto store_tile = [&](int j, const uint4 (&raw)[16]) -> bool {
+        const int it0 = 2 * j;
+        const int s0 = it0 % KSTAGES, s1 = (it0 + 1) % KSTAGES;
+        if (!tc::mbar_wait(&sm.empty[s0], ((it0 / KSTAGES) & 1) ^ 1, &sm.abort)) return false;
+        if (!tc::mbar_wait(&sm.empty[s1], (((it0 + 1) / KSTAGES) & 1) ^ 1, &sm.abort)) return false;
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int c = ct + 64 * u;
+          const int r = c >> 3, pc = c & 7;
+          uint8_t* dst = sm.kst[pc < 4 ? s0 : s1] + r * 128;
+          const int c0 = 2 * (pc & 3);                // f16 chunks c0, c0+1 of the 64-feature half
+          const uint4 x = raw[u];
+          const uint4 o0 = make_uint4(e4m3x2_to_f16x2(x.x), e4m3x2_to_f16x2(x.x >> 16), e4m3x2_to_f16x2(x.y),
+                                      e4m3x2_to_f16x2(x.y >> 16));
+          const uint4 o1 = make_uint4(e4m3x2_to_f16x2(x.z), e4m3x2_to_f16x2(x.z >> 16), e4m3x2_to_f16x2(x.w),
+                                      e4m3x2_to_f16x2(x.w >> 16));
+          *reinterpret_cast<uint4*>(dst + ((c0 ^ (r & 7)) << 4)) = o0;
+          *reinterpret_cast<uint4*>(dst + (((c0 + 1) ^ (r & 7)) << 4)) = o1;
+        }
+        tc::fence_proxy_async_smem();
+        tc::mbar_arrive(&sm.full[s0]);
+        tc::mbar_arrive(&sm.full[s1]);
+        return true;
+      };
+      // one tile's loads stay in flight while the previous one is converted
+      uint4 ra[16], rb[16];
+      bool ok = true;
+      load_tile(0, ra);
+      for (int j = 0; j < nt; j += 2) {
+        if (j + 1 < nt) load_tile(j + 1, rb);
+        if (!(ok = store_tile(j, ra))) break;
+        if (j + 1 >= nt) break;
+        if (j + 2 < nt) load_tile(j + 2, ra);
+        if (!(ok = store_tile(j + 1, rb))) break;
+      }
+      if (!ok) set_abort(sm, status);
+    }
   } else {
     // ================= epilogue: scores + streaming top-k =================
     const int wg = (warp - 2) >> 2;               // warpgroup 0 / 1
@@ -214,10 +316,59 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
     uint32_t rmin[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};  // bounds of the keys in the list
     uint32_t rmax[2] = {0u, 0u};
 
+    if constexpr (E4M3) {
+      // this warpgroup's two q rows: thread = (row q0 + wtid / 64, head wtid % 64)
+      const bool okq = tc::mbar_wait(&sm.qfull, 0, &sm.abort);
+      if (!okq) set_abort(sm, status);
+      const int qi = q0 + (wtid >> 6), hd = wtid & 63;
+      const int qr = qi * HH + hd;                  // row of the 256-row B operand
+      const int sw = qr & 7;
+      float amax = 0.0f;
+      if (okq) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            float f[8];
+            bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm.qb[hh] + qr * 128 + ((c ^ sw) << 4)), f);
+#pragma unroll
+            for (int x = 0; x < 8; ++x) amax = fmaxf(amax, fabsf(f[x]));
+          }
+      }
+      const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+      const int e = amax > 0.0f ? max(-120, min(126, 141 - ex)) : 0;
+      const float scale = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+      const float inv_scale = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+      if (okq) {
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4* p = reinterpret_cast<uint4*>(sm.qb[hh] + qr * 128 + ((c ^ sw) << 4));
+            float f[8];
+            bf16x8_to_f32(*p, f);
+            *p = make_uint4(f32x2_to_f16x2(f[0] * scale, f[1] * scale), f32x2_to_f16x2(f[2] * scale, f[3] * scale),
+                            f32x2_to_f16x2(f[4] * scale, f[5] * scale), f32x2_to_f16x2(f[6] * scale, f[7] * scale));
+          }
+        sm.wsm[qi][hd] *= inv_scale;
+      }
+      tc::fence_proxy_async_smem();
+      tc::mbar_arrive(&sm.qconv);
+      wsync();                                      // the warpgroup's scaled weights are in place
+    }
+    // e4m3: the key scales of the next tile are loaded one tile ahead
+    const float* ksrow = E4M3 ? a.kscale + static_cast<size_t>(b) * a.S_cap : nullptr;
+    float ks_next = (E4M3 && key_local < n_keys) ? __ldg(ksrow + key_local) : 1.0f;
+
     bool aborted = false;
     for (int j = 0; j < nt; ++j) {
       const int acc = j & 1;
       const int par = j & 1;
+      const float ks = ks_next;
+      if (E4M3) {
+        const int sn = (j + 1) * KT + key_local;
+        ks_next = sn < n_keys ? __ldg(ksrow + sn) : 1.0f;
+      }
       const bool ok = tc::mbar_wait(&sm.tfull[acc], (j >> 1) & 1, &sm.abort);
       if (!ok) set_abort(sm, status);
       tc::tc_fence_after();
@@ -247,7 +398,7 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
           s2 = fmaf(w4.z, fmaxf(__uint_as_float(r1[h + 2]), 0.0f), s2);
           s3 = fmaf(w4.w, fmaxf(__uint_as_float(r1[h + 3]), 0.0f), s3);
         }
-        key[qq] = float_key((s0 + s1) + (s2 + s3));
+        key[qq] = float_key(E4M3 ? ((s0 + s1) + (s2 + s3)) * ks : (s0 + s1) + (s2 + s3));
       }
       tc::tc_fence_before();
       tc::mbar_arrive(&sm.tempty[acc]);           // accumulator may be overwritten
@@ -332,7 +483,7 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
 }  // namespace
 
 bool indexer_prefill_tc_supported(const IndexerArgs& a) {
-  return a.H == HH && a.D == DD && !a.e4m3 && a.T > kDecodeMaxT;
+  return a.H == HH && a.D == DD && a.T > kDecodeMaxT && (!a.e4m3 || a.kscale != nullptr);
 }
 
 cudaError_t launch_indexer_prefill_tc(const IndexerArgs& a, int* dev_status, cudaStream_t st) {
@@ -341,16 +492,18 @@ cudaError_t launch_indexer_prefill_tc(const IndexerArgs& a, int* dev_status, cud
   if (!encode_tmap_2d(&tm_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(a.B) * a.T * HH, DD,
                       NCOL, 64))
     return cudaErrorInvalidValue;
-  if (!encode_tmap_2d(&tm_k, a.kI, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(a.B) * a.S_cap, DD,
-                      KT, 64))
+  // e4m3 keys are read with plain loads; the key map is then unused
+  if (a.e4m3) tm_k = tm_q;
+  else if (!encode_tmap_2d(&tm_k, a.kI, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(a.B) * a.S_cap,
+                           DD, KT, 64))
     return cudaErrorInvalidValue;
   const int n_groups = (a.T + QPB - 1) / QPB;
   const size_t smem = sizeof(TcSmem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(indexer_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  auto kern = a.e4m3 ? indexer_prefill_tc_kernel<true> : indexer_prefill_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(n_groups, a.B);
-  indexer_prefill_tc_kernel<<<grid, NTHREADS, smem, st>>>(tm_q, tm_k, a, n_groups, dev_status);
+  kern<<<grid, a.e4m3 ? NTHREADS_E4M3 : NTHREADS, smem, st>>>(tm_q, tm_k, a, n_groups, dev_status);
   return cudaGetLastError();
 }
 

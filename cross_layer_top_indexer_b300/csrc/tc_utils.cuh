@@ -245,6 +245,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
 }
 
+// Instruction descriptor, kind::f16: f16 A and B (K-major), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4)                                 // D format: f32 (A, B format fields 0 = f16)
+         | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
+}
+
 // Instruction descriptor, kind::f8f6f4: e4m3 A and B (K-major), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
   return (1u << 4)                                 // D format: f32 (A, B format fields 0 = e4m3)

@@ -128,7 +128,9 @@ CASES = [
     (1, 517, 517, 0, 64, 128, 1, "normal", "bf16"),          # k = 1
     (1, 3000, 3000, 0, 64, 128, 2048, "normal", "bf16"),     # k = 2048 with compactions
     (1, 600, 600, 0, 8, 32, 100, "int", "bf16"),             # heavy ties, bit-exact
-    (1, 1500, 1500, 0, 64, 128, 256, "normal", "e4m3"),      # fp8 keys
+    (1, 1500, 1500, 0, 64, 128, 256, "normal", "e4m3"),      # fp8 keys (tensor-core path)
+    (2, 700, 1700, 1000, 64, 128, 2048, "normal", "e4m3"),   # fp8 keys, chunk at an offset, batch 2
+    (1, 900, 900, 0, 16, 64, 64, "normal", "e4m3"),          # fp8 keys, mma.sync path
     (1, 1029, 1029, 0, 4, 32, 16, "int", "bf16"),            # tiny head shape, ragged
     (1, 777, 777, 0, 64, 128, 100, "int", "bf16"),           # tensor-core path, integer: bit-exact
     (2, 2600, 2600, 0, 64, 128, 2048, "int", "bf16"),        # tensor-core path, ties across cuts
@@ -149,6 +151,35 @@ def test_indexer_prefill_cases(case):
         pu.check_topk(got[b], pu.to_f64(q[b]), pu.keys_f64(kI[b], None if ks is None else ks[b]),
                       pu.to_f64(w[b]), k, q_pos0, range(T), exact=(dist == "int"), stats=stats)
     if dist != "int":
+        pu.check_recall(stats)
+
+
+@pytest.mark.parametrize("T,k,mode", [(900, 100, "int"), (1283, 512, "codes")])
+def test_prefill_e4m3_every_code(T, k, mode):
+    # e4m3 keys through the tensor-core prefill kernel: integer codes with
+    # power-of-two key scales (exact products and sums: bit-exact sets), or
+    # every code but NaN with random scales (tolerance rule)
+    g = torch.Generator(device="cpu").manual_seed(T)
+    if mode == "int":
+        ints = torch.tensor([0x00, 0x38, 0x40, 0x44, 0xB8, 0xC0, 0xC4], dtype=torch.uint8)   # 0, 1, 2, 3, -1, -2, -3
+        kb = ints[torch.randint(0, len(ints), (1, T, 128), generator=g)]
+        q = torch.randint(-2, 3, (1, T, 64, 128), generator=g).float()
+        w = torch.randint(-2, 3, (1, T, 64), generator=g).float()
+        ks = 2.0 ** torch.randint(-1, 2, (1, T), generator=g).float()
+    else:
+        codes = torch.tensor([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=torch.uint8)
+        kb = codes[torch.randint(0, len(codes), (1, T, 128), generator=g)]
+        q = torch.randn(1, T, 64, 128, generator=g) / 11.3
+        w = torch.randn(1, T, 64, generator=g) / 8
+        ks = torch.rand(1, T, generator=g) * 0.01 + 1e-3
+    kI = kb.view(torch.float8_e4m3fn).to(DEV)
+    q, w, ks = q.to(DEV, torch.bfloat16), w.to(DEV), ks.to(DEV)
+    got = _idx64(B.indexer_topk(q, kI, w, k, kscale=ks))
+    torch.cuda.synchronize()
+    stats = {"hit": 0, "tot": 0}
+    pu.check_topk(got[0], pu.to_f64(q[0]), pu.keys_f64(kI[0], ks[0]), pu.to_f64(w[0]), k, 0, range(T),
+                  exact=(mode == "int"), stats=stats)
+    if mode != "int":
         pu.check_recall(stats)
 
 
