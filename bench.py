@@ -9,10 +9,12 @@ Headline workload (one step = one pass of the whole hot path):
   sparse attention on all 47.  Inputs are seeded synthetic tensors resident
   in HBM; every layer's q_I (512 MiB) and Q (256 MiB) exceed the 126 MB L2.
 
-Also reported: the same stack all-Full (standard DSA), the end-to-end figure
-through host buffers, the decode workload (32 sequences at context 131072,
-64 steps, fp8 keys), per-kernel roofline fractions from live CUDA events, and
-the CPU oracle timed on a bounded sample (a reported baseline, not a target).
+Also reported: the same stack all-Full (standard DSA), the same 1/4-F stack
+with e4m3 indexer keys, the end-to-end figure through host buffers, the
+decode workload (32 sequences at context 131072, 64 steps, fp8 keys) with
+its kernels against HBM bandwidth, per-kernel roofline fractions from live
+CUDA events, and the CPU oracle timed on a bounded sample (a reported
+baseline, not a target).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -281,16 +283,31 @@ def run_decode(binding, pattern, steps_tok, seed, dev, gpu_index):
         torch.cuda.synchronize()
     binding.stream_status()
     ms = t0.elapsed_time(t1)
-    # per-kernel breakdown on one traced step at the last context length
-    tr = binding.Trace(len(pattern), 1)
-    fwds[-1](stream, trace=tr)
-    torch.cuda.synchronize()
-    _, idx_ms, attn_ms = tr.read()
-    tr.close()
+    # per-call breakdown at the last context length: each call alone, repeated,
+    # CUDA events on the stream (a traced step would also count launch gaps)
+    q_last = cfg.q_pos0 + steps_tok - 1
+    L0 = layers[0]
+
+    def call_ms(fn, reps):
+        fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    idx_layer_ms = call_ms(lambda: binding.indexer_topk(L0["q"], L0["kI"], L0["w"], cfg.k, q_last,
+                                                        kscale=L0["kscale"], S=q_last + 1, idx_out=cache, ws=ws,
+                                                        stream=stream), 10)
+    attn_layer_ms = call_ms(lambda: binding.sparse_attn(L0["Q"], L0["K"], L0["V"], cache, S=q_last + 1, O=L0["O"],
+                                                        ws=ws, stream=stream), 20)
+    binding.stream_status()
     del layers, fwds, ws
     torch.cuda.empty_cache()
-    idx_layer_ms = sum(idx_ms) / max(1, pattern.count("F"))
-    attn_layer_ms = sum(attn_ms) / len(pattern)
     # algorithmic HBM bytes of one layer at the traced context S = S_cap:
     # indexer: every cached key once (d_I e4m3 bytes + its fp32 scale) plus q, w
     # and the index row; attention: the k selected K and V rows (bf16) plus Q, O
@@ -467,6 +484,23 @@ def ours_arm(args, world, rank, local):
     del layers, fwd
     torch.cuda.empty_cache()
 
+    # ---- the same 1/4-F stack with e4m3 indexer keys (per-key fp32 scale) ----
+    e4 = None
+    if not args.no_e4m3:
+        cfg8 = cfg.with_(k_dtype="e4m3")
+        layers8 = make_prefill_layers(cfg8, seed + 3, dev, "pattern")
+        fwd8 = binding.Forward(quarter, layers8, cfg.k)
+        barrier(world)
+        k8 = max(2, args.steps // 2)
+        t8, per8, clk8 = time_forward(binding, fwd8, k8, max(1, args.warmup // 2), cfg.n_layers, gpu_index)
+        t8 = reduce_max(t8, world)
+        ms8 = t8 / k8
+        e4 = {"pattern": quarter, "k_dtype": "e4m3", "ms_per_step": ms8,
+              "value": world * cfg.B * cfg.T / (ms8 * 1e-3), "unit": "tok/s", "steps": k8,
+              "kernels": kernel_roofline(per8, quarter, cfg, peaks, k8), "clocks": clk8}
+        del layers8, fwd8
+        torch.cuda.empty_cache()
+
     decode = None
     if not args.no_decode:
         dq = run_decode(binding, synth.DECODE.pattern, args.decode_steps, seed + 1, dev, gpu_index)
@@ -503,7 +537,7 @@ def ours_arm(args, world, rank, local):
                        "l2": "inputs larger than L2 (per layer q_I 512 MiB, Q 256 MiB; 126 MB L2), no flush"},
             "roofline": roofline, "kernels": kern, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": args.steps * launches_per_forward(quarter, cfg.B, cfg.T, cfg.k),
-            "clocks": clocks, "all_f": allf_res,
+            "clocks": clocks, "all_f": allf_res, "e4m3_keys": e4,
             "speedup_quarter_vs_allf": (value / allf_res["value"]) if allf_res else None,
             "decode": decode, "peaks": {k: v for k, v in peaks.items() if not k.startswith("_") and
                                         isinstance(v, (int, float))}}
@@ -519,6 +553,7 @@ def main():
     ap.add_argument("--no-allf", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e4m3", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--decode-steps", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
