@@ -98,7 +98,7 @@ ic_status check_attn(int B, int T, int S, int S_cap, int Hq, int Dh, int k, cons
 }
 
 size_t indexer_ws(int B, int T, int S) {
-  return T <= ic::kDecodeMaxT ? ic::indexer_decode_ws_bytes(B, T, S) : 0;
+  return T <= ic::kDecodeMaxT ? ic::indexer_decode_ws_fast_bytes(B, T, S) : 0;
 }
 
 ic_status cuda_fail(cudaError_t e, const char* what) {

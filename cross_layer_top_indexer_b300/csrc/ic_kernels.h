@@ -38,15 +38,23 @@ cudaError_t launch_indexer_prefill(const IndexerArgs& a, int* dev_status, cudaSt
 bool encode_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int elt_bytes, uint64_t rows,
                     uint64_t cols, uint32_t box_rows, uint32_t box_cols);
 
-// Decode indexer: score rows into ws, then an exact radix select per row.
+// Decode indexer: score rows into ws, then an exact select per row.
+// indexer_decode_ws_bytes is the least workspace the path needs (the score
+// rows); indexer_decode_ws_fast_bytes adds the histogram, chunk counts and
+// candidate buffers of the chunked select, which the path uses when the
+// workspace holds them.
 size_t indexer_decode_ws_bytes(int B, int T, int S);
+size_t indexer_decode_ws_fast_bytes(int B, int T, int S);
 cudaError_t launch_indexer_decode(const IndexerArgs& a, void* ws, size_t ws_bytes, int* dev_status,
                                   cudaStream_t st);
 // Rows per sequence at or below which the indexer takes the decode path.
 constexpr int kDecodeMaxT = 8;
+// Decode select: bins of the score-key histogram the decode scorer builds
+// (the top kDecHistBits bits of the order-preserving key).
+constexpr int kDecHistBits = 11;
 // Tensor-core decode scores for one query row per sequence, H = 64, D = 128:
 bool indexer_decode_tc_supported(const IndexerArgs& a);
-cudaError_t launch_indexer_decode_tc(const IndexerArgs& a, float* scores, size_t pitch, int* dev_status,
+cudaError_t launch_indexer_decode_tc(const IndexerArgs& a, float* scores, size_t pitch, int* hist, int* dev_status,
                                      cudaStream_t st);
 
 // Sparse attention; splits the k rows over CTAs (partials in ws) when few rows.

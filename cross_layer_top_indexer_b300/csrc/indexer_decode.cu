@@ -416,6 +416,188 @@ cudaError_t launch_select(float* scores, size_t pitch, const IndexerArgs& a, cud
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Chunked select (one query row per sequence, after the tensor-core scorer,
+// which leaves a histogram of each row's score keys by their top
+// kDecHistBits bits).  The threshold bin is the bin of the k-th largest key;
+// the entries in and above it are the candidates.
+//   select_chunk_kernel   one CTA per (chunk of CH scores, row): writes the
+//                         positions of its candidates, in order, to the
+//                         chunk's region and their count
+//   select_finish_kernel  one CTA per row: gathers the candidates in chunk
+//                         order (= position order) into shared memory with
+//                         their keys and cuts them to exactly k
+// Rows with more candidates than FCAP take the general radix path.
+// ---------------------------------------------------------------------------
+constexpr int HBINS = 1 << kDecHistBits;
+constexpr int CH = 4096;                 // scores per chunk
+constexpr int CTHREADS = 256;            // 16 scores per thread
+constexpr int FCH = 2048;                // chunks per row the finish kernel indexes (rows up to 8 Mi keys)
+
+struct DecWs {
+  float* scores;
+  int* hist;    // [rows][HBINS]
+  int* cnt;     // [rows][nch]
+  int* cand;    // [rows][nch][CH]
+  size_t pitch;
+  int nch;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+DecWs carve_ws(void* ws, int rows, int S, size_t* total) {
+  DecWs d;
+  d.pitch = row_pitch(S);
+  d.nch = static_cast<int>((d.pitch + CH - 1) / CH);
+  unsigned char* p = static_cast<unsigned char*>(ws);
+  size_t off = 0;
+  d.scores = reinterpret_cast<float*>(p + off);
+  off += align256(static_cast<size_t>(rows) * d.pitch * sizeof(float));
+  d.hist = reinterpret_cast<int*>(p + off);
+  off += align256(static_cast<size_t>(rows) * HBINS * sizeof(int));
+  d.cnt = reinterpret_cast<int*>(p + off);
+  off += align256(static_cast<size_t>(rows) * d.nch * sizeof(int));
+  d.cand = reinterpret_cast<int*>(p + off);
+  off += align256(static_cast<size_t>(rows) * d.nch * CH * sizeof(int));
+  *total = off;
+  return d;
+}
+
+// Threshold bin of a row from its histogram: the bin b* with
+// count(bins > b*) < k <= count(bins >= b*); *ncand = count(bins >= b*).
+// All NT threads call it; NT * BPT == HBINS.
+template <int NT>
+__device__ void threshold_bin(const int* h, int k, int* warp_sums, int* s_bsel, int* s_ncand) {
+  constexpr int BPT = HBINS / NT;
+  const int tid = threadIdx.x;
+  if (tid == 0) { *s_bsel = 0; *s_ncand = 0x7FFFFFFF; }   // a histogram short of k sends the row to the radix path
+  int c[BPT];
+  int s = 0;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) { c[j] = h[HBINS - 1 - BPT * tid - j]; s += c[j]; }
+  int total;
+  const int excl = block_exclusive_scan(s, warp_sums, NT, total, tid, BlockSync());
+  if (excl < k && k <= excl + s) {
+    int cum = excl;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) {
+      if (cum + c[j] >= k) { *s_bsel = HBINS - 1 - BPT * tid - j; *s_ncand = cum + c[j]; break; }
+      cum += c[j];
+    }
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(CTHREADS)
+select_chunk_kernel(const float* scores, size_t pitch, const int* hist, int* cnt, int* cand, int nch, int n, int k) {
+  __shared__ int warp_sums[32];
+  __shared__ int s_bsel, s_ncand;
+  const int row = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+  if (n <= k) return;                            // the finish kernel writes 0 .. n-1
+  threshold_bin<CTHREADS>(hist + static_cast<size_t>(row) * HBINS, k, warp_sums, &s_bsel, &s_ncand);
+  if (s_ncand > FCAP) return;                    // the finish kernel takes the radix path
+  const uint32_t lo = static_cast<uint32_t>(s_bsel) << (32 - kDecHistBits);
+  const float* sc = scores + static_cast<size_t>(row) * pitch;
+  const int i0 = c * CH + 16 * tid;
+  float v[16];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float4 x = load_row4(sc, i0 + 4 * j, n);
+    v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
+  }
+  unsigned f = 0;
+  int cl = 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (i0 + j < n && float_key(v[j]) >= lo) { f |= 1u << j; ++cl; }
+  int tot;
+  int off = block_exclusive_scan(cl, warp_sums, CTHREADS, tot, tid, BlockSync());
+  int* dst = cand + (static_cast<size_t>(row) * nch + c) * CH;
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    if (f & (1u << j)) dst[off++] = i0 + j;
+  if (tid == 0) cnt[static_cast<size_t>(row) * nch + c] = tot;
+}
+
+struct FinishSmem {
+  uint32_t key[FCAP];
+  int pos[FCAP];
+  int coff[FCH + 1];
+  SelectScratch scr;
+  int bsel, ncand;
+};
+
+__global__ void __launch_bounds__(STHREADS)
+select_finish_kernel(const float* scores, size_t pitch, const int* hist, const int* cnt, const int* cand, int nch,
+                     int32_t* idx, int n, int k) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  FinishSmem& sm = *reinterpret_cast<FinishSmem*>(smem_raw);
+  const int row = blockIdx.x, tid = threadIdx.x;
+  const float* sc = scores + static_cast<size_t>(row) * pitch;
+  int32_t* out = idx + static_cast<size_t>(row) * k;
+  if (n <= k) {
+    for (int j = tid; j < k; j += STHREADS) out[j] = j < n ? j : -1;
+    return;
+  }
+  threshold_bin<STHREADS>(hist + static_cast<size_t>(row) * HBINS, k, sm.scr.warp_sums, &sm.bsel, &sm.ncand);
+  const int ncand = sm.ncand;
+  const int nc = (n + CH - 1) / CH;              // chunks of this row
+  if (ncand > FCAP || nc > FCH) {
+    radix_select_row(sc, n, k, out);
+    return;
+  }
+  // chunk offsets (exclusive prefix of the counts), then the candidates in order
+  const int* crow = cnt + static_cast<size_t>(row) * nch;
+  int run = 0;
+  for (int c0 = 0; c0 < nc; c0 += STHREADS) {
+    const int v = c0 + tid < nc ? crow[c0 + tid] : 0;
+    int tot;
+    const int ex = block_exclusive_scan(v, sm.scr.warp_sums, STHREADS, tot, tid, BlockSync());
+    if (c0 + tid < nc) sm.coff[c0 + tid] = run + ex;
+    run += tot;
+  }
+  if (tid == 0) sm.coff[nc] = run;
+  __syncthreads();
+  if (run != ncand) {                            // counts disagree with the histogram: take the general path
+    radix_select_row(sc, n, k, out);
+    return;
+  }
+  const int* crand = cand + static_cast<size_t>(row) * nch * CH;
+  for (int i = tid; i < ncand; i += STHREADS) {
+    int lo = 0, hi = nc;                         // largest c with coff[c] <= i
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sm.coff[mid] <= i) lo = mid; else hi = mid;
+    }
+    const int p = crand[static_cast<size_t>(lo) * CH + (i - sm.coff[lo])];
+    sm.pos[i] = p;
+    sm.key[i] = float_key(sc[p]);
+  }
+  __syncthreads();
+  if (ncand > k) {
+    uint32_t thr;
+    const uint32_t lo_key = static_cast<uint32_t>(sm.bsel) << (32 - kDecHistBits);
+    cut_list<STHREADS, FSEG>(sm.key, sm.pos, ncand, k, k, lo_key, 0xFFFFFFFFu, &sm.scr, tid, BlockSync(), &thr);
+  }
+  for (int j = tid; j < k; j += STHREADS) out[j] = sm.pos[j];
+}
+
+cudaError_t launch_chunked_select(const DecWs& d, const IndexerArgs& a, cudaStream_t st) {
+  const int n = a.q_pos0 + 1;                    // one row per sequence (T = 1)
+  if (n > a.k) {
+    dim3 g1((n + CH - 1) / CH, a.B);
+    select_chunk_kernel<<<g1, CTHREADS, 0, st>>>(d.scores, d.pitch, d.hist, d.cnt, d.cand, d.nch, n, a.k);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const size_t smem = sizeof(FinishSmem);
+  cudaError_t e = cudaFuncSetAttribute(select_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  select_finish_kernel<<<a.B, STHREADS, smem, st>>>(d.scores, d.pitch, d.hist, d.cnt, d.cand, d.nch, a.idx, n, a.k);
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch_scores(const IndexerArgs& a, float* scores, size_t pitch, cudaStream_t st) {
   const int h_pad = ((a.H + 15) / 16) * 16;
@@ -433,6 +615,12 @@ cudaError_t launch_scores(const IndexerArgs& a, float* scores, size_t pitch, cud
 
 size_t indexer_decode_ws_bytes(int B, int T, int S) { return (size_t)B * T * row_pitch(S) * sizeof(float); }
 
+size_t indexer_decode_ws_fast_bytes(int B, int T, int S) {
+  size_t total = 0;
+  carve_ws(nullptr, B * T, S, &total);
+  return total;
+}
+
 cudaError_t launch_indexer_decode(const IndexerArgs& a, void* ws, size_t ws_bytes, int* dev_status,
                                   cudaStream_t st) {
   if (ws_bytes < indexer_decode_ws_bytes(a.B, a.T, a.S)) return cudaErrorInvalidValue;
@@ -440,7 +628,17 @@ cudaError_t launch_indexer_decode(const IndexerArgs& a, void* ws, size_t ws_byte
   const size_t pitch = row_pitch(a.S);
   cudaError_t e;
   if (indexer_decode_tc_supported(a)) {
-    e = launch_indexer_decode_tc(a, scores, pitch, dev_status, st);
+    size_t need = 0;
+    const DecWs d = carve_ws(ws, a.B * a.T, a.S, &need);
+    if (ws_bytes >= need) {
+      // histogram built by the scorer, then the chunked select
+      e = cudaMemsetAsync(d.hist, 0, static_cast<size_t>(a.B) * a.T * HBINS * sizeof(int), st);
+      if (e != cudaSuccess) return e;
+      e = launch_indexer_decode_tc(a, scores, pitch, d.hist, dev_status, st);
+      if (e != cudaSuccess) return e;
+      return launch_chunked_select(d, a, st);
+    }
+    e = launch_indexer_decode_tc(a, scores, pitch, nullptr, dev_status, st);
     if (e != cudaSuccess) return e;
     return launch_select(scores, pitch, a, st);
   }

@@ -7,8 +7,12 @@
 // page "NLP--IndexCache", section "背景 & 问题提出"):
 //     I[b,s] = k_scale[b,s] * sum_h w[b,h] * ReLU(q[b,h,:] . kI[b,s,:]),  s <= pos
 // (a positive scale commutes with ReLU).  One fp32 score row per sequence
-// goes to the workspace, and the radix-select kernel of the decode path
-// picks the top k from it.
+// goes to the workspace, and the select kernels of the decode path pick the
+// top k from it.  When given a histogram buffer, the kernel also counts the
+// scores of each sequence by the top kDecHistBits bits of their order-
+// preserving key (a shared-memory histogram per epilogue warpgroup, added
+// into the global one at the end of each sequence), which lets the select
+// find its threshold without a pass over the row.
 //
 // e4m3 keys go to the tensor cores as they are stored (kind::f8f6f4), so no
 // thread touches a key byte.  The bf16 query is carried exactly by two e4m3
@@ -63,6 +67,7 @@ constexpr int NTHREADS = 12 * 32;
 constexpr int PREP_THREADS = 64;         // thread = head
 constexpr int EPI_GROUPS = 2;
 constexpr int EPI_THREADS = 128;         // per group
+constexpr int HBINS = 1 << kDecHistBits;
 constexpr uint32_t IDESC_BF16 = tc::idesc_bf16_f32(KT, HH);
 constexpr uint32_t IDESC_E4M3 = tc::idesc_e4m3_f32(KT, 2 * HH);
 
@@ -71,6 +76,7 @@ struct __align__(1024) DecTcSmem {
   uint8_t qs[2][2][HH * 128];            // bf16 q of a sequence: two 64-feature halves, 64 rows x 128 B (SW128)
   uint8_t qsp[2][2 * HH * 128];          // e4m3 q split: hi rows 0-63, lo rows 64-127, 128 B each (SW128)
   float wsm[2][HH];                      // per-head weight (times 2^-e_h for e4m3)
+  int hist[EPI_GROUPS][HBINS];           // per epilogue warpgroup: score keys of the current sequence
   uint64_t kfull[RSTAGES], kempty[RSTAGES];
   uint64_t qfull[2], qempty[2];          // bf16 q buffer
   uint64_t pfull[2], pempty[2];          // q split + weights ready / split free
@@ -114,7 +120,7 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& c, float* f) {
 template <bool E4M3>
 __global__ void __launch_bounds__(NTHREADS, 1)
 indexer_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                         IndexerArgs a, float* scores, size_t pitch, int ntile, int* status) {
+                         IndexerArgs a, float* scores, size_t pitch, int* hist, int ntile, int* status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   DecTcSmem& sm = *reinterpret_cast<DecTcSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -127,6 +133,7 @@ indexer_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
   const long long u1 = total * (blockIdx.x + 1) / gridDim.x;
   const int n_it = static_cast<int>(u1 - u0);
   const int pos = a.q_pos0;                // the query row's position (T = 1)
+  for (int i = tid; i < EPI_GROUPS * HBINS; i += NTHREADS) (&sm.hist[0][0])[i] = 0;
 
   if (tid == 0) {
     for (int s = 0; s < RSTAGES; ++s) { tc::mbar_init(&sm.kfull[s], 1); tc::mbar_init(&sm.kempty[s], 1); }
@@ -333,76 +340,102 @@ indexer_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
       return (e4m3 && j < n_it && ps <= pos) ? __ldg(a.kscale + static_cast<size_t>(pb) * a.S_cap + ps) : 1.0f;
     };
     float ks_a = scale_at(grp), ks_b = scale_at(grp + EPI_GROUPS);
-    for (int i = 0; ok && i < n_it; ++i, kt = kt + 1 == ntile ? 0 : kt + 1, b += kt == 0) {
+    // A thread whose wait gives up stops working but stays in the loop until
+    // the end of the sequence, where the warpgroup decides together (one
+    // barrier vote) to stop, so that no thread is left at a barrier.
+    const int etid = (tid - 128) & (EPI_THREADS - 1);
+    for (int i = 0; i < n_it; ++i, kt = kt + 1 == ntile ? 0 : kt + 1, b += kt == 0) {
       const bool last_of_seq = i + 1 == n_it || kt + 1 == ntile;
       if (b != cur_b) {
         wb = nseq & 1;
-        if (!tc::mbar_wait(&sm.pfull[wb], (nseq >> 1) & 1, &sm.abort)) { ok = false; break; }
+        if (ok && !tc::mbar_wait(&sm.pfull[wb], (nseq >> 1) & 1, &sm.abort)) { ok = false; set_abort(sm, status); }
         cur_b = b;
         ++nseq;
       }
-      if (i % EPI_GROUPS != grp) {
-        if (last_of_seq) tc::mbar_arrive(&sm.wempty[wb]);
-        continue;
-      }
-      const int s = kt * KT + kl;
-      const bool valid = s <= pos;
-      const float ks = ks_a;
-      ks_a = ks_b;
-      ks_b = scale_at(i + 2 * EPI_GROUPS);
-      const int acc = i % NACC;
-      if (!tc::mbar_wait(&sm.afull[acc], (i / NACC) & 1, &sm.abort)) { ok = false; break; }
-      tc::tc_fence_after();
-      const uint32_t ta = tmem + lane_field + acc * ACC_COLS;
-      const float* wq = sm.wsm[wb];
-      float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
-      if (e4m3) {
+      if (ok && i % EPI_GROUPS == grp) {
+        const int s = kt * KT + kl;
+        const bool valid = s <= pos;
+        const float ks = ks_a;
+        ks_a = ks_b;
+        ks_b = scale_at(i + 2 * EPI_GROUPS);
+        const int acc = i % NACC;
+        if (!tc::mbar_wait(&sm.afull[acc], (i / NACC) & 1, &sm.abort)) {
+          ok = false;
+          set_abort(sm, status);
+        } else {
+          tc::tc_fence_after();
+          const uint32_t ta = tmem + lane_field + acc * ACC_COLS;
+          const float* wq = sm.wsm[wb];
+          float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;
+          if (e4m3) {
 #pragma unroll
-        for (int hb = 0; hb < HH; hb += 32) {         // heads hb .. hb+31: hi columns, then lo columns
-          uint32_t hi[32], lo[32];
-          tc::tmem_ld_x32(ta + hb, hi);
-          tc::tmem_ld_x32(ta + HH + hb, lo);
-          tc::tmem_wait_ld();
-          if (hb + 32 == HH) {
+            for (int hb = 0; hb < HH; hb += 32) {         // heads hb .. hb+31: hi columns, then lo columns
+              uint32_t hi[32], lo[32];
+              tc::tmem_ld_x32(ta + hb, hi);
+              tc::tmem_ld_x32(ta + HH + hb, lo);
+              tc::tmem_wait_ld();
+              if (hb + 32 == HH) {
+                tc::tc_fence_before();
+                tc::mbar_arrive(&sm.aempty[acc]);
+              }
+#pragma unroll
+              for (int h = 0; h < 32; h += 4) {
+                const float4 w4 = *reinterpret_cast<const float4*>(wq + hb + h);
+                s0 = fmaf(w4.x, fmaxf(__uint_as_float(hi[h + 0]) + __uint_as_float(lo[h + 0]), 0.0f), s0);
+                s1 = fmaf(w4.y, fmaxf(__uint_as_float(hi[h + 1]) + __uint_as_float(lo[h + 1]), 0.0f), s1);
+                s2 = fmaf(w4.z, fmaxf(__uint_as_float(hi[h + 2]) + __uint_as_float(lo[h + 2]), 0.0f), s2);
+                s3 = fmaf(w4.w, fmaxf(__uint_as_float(hi[h + 3]) + __uint_as_float(lo[h + 3]), 0.0f), s3);
+              }
+            }
+          } else {
+            uint32_t r0[32], r1[32];
+            tc::tmem_ld_x32(ta, r0);
+            tc::tmem_ld_x32(ta + 32, r1);
+            tc::tmem_wait_ld();
             tc::tc_fence_before();
             tc::mbar_arrive(&sm.aempty[acc]);
+#pragma unroll
+            for (int h = 0; h < 32; h += 4) {
+              const float4 w4 = *reinterpret_cast<const float4*>(wq + h);
+              s0 = fmaf(w4.x, fmaxf(__uint_as_float(r0[h + 0]), 0.0f), s0);
+              s1 = fmaf(w4.y, fmaxf(__uint_as_float(r0[h + 1]), 0.0f), s1);
+              s2 = fmaf(w4.z, fmaxf(__uint_as_float(r0[h + 2]), 0.0f), s2);
+              s3 = fmaf(w4.w, fmaxf(__uint_as_float(r0[h + 3]), 0.0f), s3);
+            }
+#pragma unroll
+            for (int h = 0; h < 32; h += 4) {
+              const float4 w4 = *reinterpret_cast<const float4*>(wq + 32 + h);
+              s0 = fmaf(w4.x, fmaxf(__uint_as_float(r1[h + 0]), 0.0f), s0);
+              s1 = fmaf(w4.y, fmaxf(__uint_as_float(r1[h + 1]), 0.0f), s1);
+              s2 = fmaf(w4.z, fmaxf(__uint_as_float(r1[h + 2]), 0.0f), s2);
+              s3 = fmaf(w4.w, fmaxf(__uint_as_float(r1[h + 3]), 0.0f), s3);
+            }
           }
-#pragma unroll
-          for (int h = 0; h < 32; h += 4) {
-            const float4 w4 = *reinterpret_cast<const float4*>(wq + hb + h);
-            s0 = fmaf(w4.x, fmaxf(__uint_as_float(hi[h + 0]) + __uint_as_float(lo[h + 0]), 0.0f), s0);
-            s1 = fmaf(w4.y, fmaxf(__uint_as_float(hi[h + 1]) + __uint_as_float(lo[h + 1]), 0.0f), s1);
-            s2 = fmaf(w4.z, fmaxf(__uint_as_float(hi[h + 2]) + __uint_as_float(lo[h + 2]), 0.0f), s2);
-            s3 = fmaf(w4.w, fmaxf(__uint_as_float(hi[h + 3]) + __uint_as_float(lo[h + 3]), 0.0f), s3);
+          const float sc = ((s0 + s1) + (s2 + s3)) * ks;
+          if (valid) {
+            scores[static_cast<size_t>(b) * pitch + s] = sc;
+            if (hist) atomicAdd(&sm.hist[grp][float_key(sc) >> (32 - kDecHistBits)], 1);
           }
-        }
-      } else {
-        uint32_t r0[32], r1[32];
-        tc::tmem_ld_x32(ta, r0);
-        tc::tmem_ld_x32(ta + 32, r1);
-        tc::tmem_wait_ld();
-        tc::tc_fence_before();
-        tc::mbar_arrive(&sm.aempty[acc]);
-#pragma unroll
-        for (int h = 0; h < 32; h += 4) {
-          const float4 w4 = *reinterpret_cast<const float4*>(wq + h);
-          s0 = fmaf(w4.x, fmaxf(__uint_as_float(r0[h + 0]), 0.0f), s0);
-          s1 = fmaf(w4.y, fmaxf(__uint_as_float(r0[h + 1]), 0.0f), s1);
-          s2 = fmaf(w4.z, fmaxf(__uint_as_float(r0[h + 2]), 0.0f), s2);
-          s3 = fmaf(w4.w, fmaxf(__uint_as_float(r0[h + 3]), 0.0f), s3);
-        }
-#pragma unroll
-        for (int h = 0; h < 32; h += 4) {
-          const float4 w4 = *reinterpret_cast<const float4*>(wq + 32 + h);
-          s0 = fmaf(w4.x, fmaxf(__uint_as_float(r1[h + 0]), 0.0f), s0);
-          s1 = fmaf(w4.y, fmaxf(__uint_as_float(r1[h + 1]), 0.0f), s1);
-          s2 = fmaf(w4.z, fmaxf(__uint_as_float(r1[h + 2]), 0.0f), s2);
-          s3 = fmaf(w4.w, fmaxf(__uint_as_float(r1[h + 3]), 0.0f), s3);
         }
       }
-      // the weights of this sequence are no longer read after its last tile
-      if (last_of_seq) tc::mbar_arrive(&sm.wempty[wb]);
-      if (valid) scores[static_cast<size_t>(b) * pitch + s] = ((s0 + s1) + (s2 + s3)) * ks;
+      if (last_of_seq) {
+        if (hist) {
+          const bool stop = tc::named_sync_or(1 + grp, EPI_THREADS, !ok || sm.abort != 0);
+          if (!stop) {
+            int* hg = hist + static_cast<size_t>(b) * HBINS;
+            for (int bin = etid; bin < HBINS; bin += EPI_THREADS) {
+              const int v = sm.hist[grp][bin];
+              if (v) { atomicAdd(hg + bin, v); sm.hist[grp][bin] = 0; }
+            }
+          }
+          tc::named_sync(1 + grp, EPI_THREADS);   // the group's bins are clear before the next sequence
+          if (stop) break;
+        } else if (!ok) {
+          break;
+        }
+        // the weights of this sequence are no longer read by this group
+        tc::mbar_arrive(&sm.wempty[wb]);
+      }
     }
     if (!ok) set_abort(sm, status);
   }
@@ -420,7 +453,7 @@ bool indexer_decode_tc_supported(const IndexerArgs& a) {
          static_cast<long long>(a.B) * HH < (1ll << 31);
 }
 
-cudaError_t launch_indexer_decode_tc(const IndexerArgs& a, float* scores, size_t pitch, int* dev_status,
+cudaError_t launch_indexer_decode_tc(const IndexerArgs& a, float* scores, size_t pitch, int* hist, int* dev_status,
                                      cudaStream_t st) {
   CUtensorMap tm_q, tm_k;
   if (!encode_tmap_2d(&tm_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(a.B) * HH, DD, HH, 64))
@@ -439,7 +472,7 @@ cudaError_t launch_indexer_decode_tc(const IndexerArgs& a, float* scores, size_t
   auto kern = a.e4m3 ? indexer_decode_tc_kernel<true> : indexer_decode_tc_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, NTHREADS, smem, st>>>(tm_q, tm_k, a, scores, pitch, ntile, dev_status);
+  kern<<<grid, NTHREADS, smem, st>>>(tm_q, tm_k, a, scores, pitch, hist, ntile, dev_status);
   return cudaGetLastError();
 }
 

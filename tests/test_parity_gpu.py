@@ -291,6 +291,24 @@ def test_decode_select_ties(S, n_top, top_val):
         pu.check_topk(got[b], pu.to_f64(q[b]), pu.to_f64(kI[b]), pu.to_f64(w[b]), k, S - 1, [0], exact=True)
 
 
+def test_decode_select_paths_agree():
+    # the chunked select (workspace with histogram and candidate buffers) and
+    # the one-CTA select (workspace of the score rows only) pick the same rows
+    dc = synth.DECODE.with_(B=3)
+    S = 40000
+    q, kI, ks, w = synth.make_indexer_inputs(dc, 0, 23, DEV, T=1, S=S)
+    full = _idx64(B.indexer_topk(q, kI, w, 2048, S - 1, kscale=ks, S=S))
+    small_ws = torch.empty(3 * ((S + 3) // 4) * 4 * 4, dtype=torch.uint8, device=DEV)
+    small = _idx64(B.indexer_topk(q, kI, w, 2048, S - 1, kscale=ks, S=S, ws=small_ws))
+    torch.cuda.synchronize()
+    assert np.array_equal(full, small)
+    stats = {"hit": 0, "tot": 0}
+    for b in range(3):
+        pu.check_topk(full[b], pu.to_f64(q[b]), pu.keys_f64(kI[b], ks[b]), pu.to_f64(w[b]), 2048, S - 1, [0],
+                      exact=False, stats=stats)
+    pu.check_recall(stats)
+
+
 def test_decode_matches_prefill_row():
     # the decode kernels at position p give the prefill kernel's row p
     cfg = synth.StackConfig("x", 1, "F", 1, 1200, 1200, 64, 128, 128, 32, 128)
