@@ -375,6 +375,26 @@ def _attn_case(Bn, T, S, S_cap, k, mode, seed):
 
 
 @pytest.mark.parametrize("Bn,T,S,S_cap,k,mode", [
+    (32, 1, 5000, 5100, 2048, "normal"),      # the decode workload's shape: 32 rows, k = 2048
+    (5, 2, 3000, 3000, 333, "normal"),        # k not a multiple of the 64-position chunk, two rows per sequence
+    (3, 1, 700, 700, 100, "spike"),           # one dominant key
+    (4, 1, 2000, 2000, 1024, "growing"),      # later splits hold the larger scores
+    (6, 1, 3000, 3000, 512, "masked_head"),   # an empty first chunk, empty rows, out-of-range slots
+])
+def test_decode_attention_split_cases(Bn, T, S, S_cap, k, mode):
+    # few rows: the k positions are split across CTAs and the splits merged
+    Q, K, V, idx = _attn_case(Bn, T, S, S_cap, k, mode, 19)
+    O = B.sparse_attn(Q, K, V, idx, S=S)
+    torch.cuda.synchronize()
+    B.stream_status()
+    idx_o = torch.where((idx >= 0) & (idx < S), idx, torch.full_like(idx, -1))
+    for b in range(Bn):
+        pu.check_attention(O[b], Q[b], K[b, :S], V[b, :S], idx_o[b], 1.0 / math.sqrt(128))
+    if mode == "masked_head":
+        assert torch.all(O[:, ::9] == 0)
+
+
+@pytest.mark.parametrize("Bn,T,S,S_cap,k,mode", [
     (1, 296, 5000, 5000, 2048, "normal"),     # tensor-core path at its smallest row count
     (2, 200, 3000, 3100, 300, "normal"),      # k not a multiple of the 128-key tile, S_cap > S
     (1, 400, 6000, 6000, 2048, "growing"),    # the reference max rises tile after tile
