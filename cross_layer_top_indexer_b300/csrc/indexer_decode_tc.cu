@@ -33,9 +33,11 @@
 // contiguous range of (sequence, 128-key tile) pairs, and
 //   warp 0      TMA: key tiles (e4m3: 128 rows x 128 B, eight stages; bf16:
 //               two 64-feature halves, four stages), and each sequence's q
-//   warp 1      MMA into one of four TMEM accumulators (keys on the lanes,
-//               heads on the columns)
-//   warps 2-3   per sequence: the q split above (e4m3) and the head weights
+//   warps 1, 3  MMA issuers, alternate tiles, into four TMEM accumulators
+//               (keys on the lanes, heads on the columns): the issue of a
+//               tcgen05.mma holds its thread for about as long as a small MMA
+//               runs, so two issuers keep the tensor core busier
+//   warp 2      per sequence: the q split above (e4m3) and the head weights
 //   warps 4-11  epilogue, two warpgroups taking alternate tiles: thread =
 //               key; the weighted ReLU sum of its 64 heads, times the key's
 //               scale, written to the score row
@@ -64,7 +66,8 @@ constexpr int NACC = 4;                  // TMEM accumulators
 constexpr int ACC_COLS = 2 * HH;         // 128 columns each (bf16 keys use the first 64)
 constexpr uint32_t TMEM_COLS = NACC * ACC_COLS;
 constexpr int NTHREADS = 12 * 32;
-constexpr int PREP_THREADS = 64;         // thread = head
+constexpr int PREP_THREADS = 32;         // thread = two heads
+constexpr int MMA_ISSUERS = 2;           // warps 1 and 3, alternate tiles
 constexpr int EPI_GROUPS = 2;
 constexpr int EPI_THREADS = 128;         // per group
 constexpr int HBINS = 1 << kDecHistBits;
@@ -139,13 +142,13 @@ indexer_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
     for (int s = 0; s < RSTAGES; ++s) { tc::mbar_init(&sm.kfull[s], 1); tc::mbar_init(&sm.kempty[s], 1); }
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(&sm.qfull[s], 1);
-      tc::mbar_init(&sm.qempty[s], e4m3 ? PREP_THREADS : 1);
+      tc::mbar_init(&sm.qempty[s], e4m3 ? PREP_THREADS : MMA_ISSUERS);
       tc::mbar_init(&sm.pfull[s], PREP_THREADS);
-      tc::mbar_init(&sm.pempty[s], 1);
+      tc::mbar_init(&sm.pempty[s], MMA_ISSUERS);
       tc::mbar_init(&sm.wempty[s], EPI_GROUPS * EPI_THREADS);
     }
     for (int s = 0; s < NACC; ++s) { tc::mbar_init(&sm.afull[s], 1); tc::mbar_init(&sm.aempty[s], EPI_THREADS); }
-    tc::mbar_init(&sm.drain, 1);
+    tc::mbar_init(&sm.drain, MMA_ISSUERS);
     sm.abort = 0;
     tc::fence_mbar_init();
   }
@@ -198,8 +201,9 @@ indexer_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
         tc::mbar_wait(&sm.qfull[n & 1], (n >> 1) & 1, nullptr);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ================= MMA issuer =================
+  } else if (warp == 1 || warp == 3) {
+    // ================= MMA issuers (tile i: issuer i % 2) =================
+    const int mi = warp == 1 ? 0 : 1;
     if (lane == 0) {
       bool ok = true;
       int nseq = 0, cur_b = -1, qb = 0;
@@ -221,6 +225,7 @@ indexer_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
           cur_b = b;
           ++nseq;
         }
+        if (i % MMA_ISSUERS == mi) {
         const int acc = i % NACC;
         const int s = i % nst;
         if (!tc::mbar_wait(&sm.aempty[acc], ((i / NACC) & 1) ^ 1, &sm.abort)) { ok = false; break; }
@@ -243,7 +248,8 @@ indexer_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
         }
         tc::mma_commit(&sm.kempty[s]);
         tc::mma_commit(&sm.afull[acc]);
-        // the q operand of this sequence is free once these MMAs are done
+        }
+        // the q operand of this sequence is free once both issuers' MMAs on it are done
         if (last_of_seq) tc::mma_commit(e4m3 ? &sm.pempty[qb] : &sm.qempty[qb]);
       }
       if (!ok) set_abort(sm, status);
@@ -251,10 +257,8 @@ indexer_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
       if (!tc::mbar_wait(&sm.drain, 0, nullptr, 4000000000ull)) set_abort(sm, status);
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // ================= per-sequence q split and weights (thread = head) =================
-    const int h = tid - 64;                         // 0..63
-    const int sw = h & 7;
+  } else if (warp == 2) {
+    // ================= per-sequence q split and weights (thread = heads lane, lane + 32) =================
     bool ok = true;
     if (n_it > 0) {
       const int b_first = static_cast<int>(u0 / ntile), b_last = static_cast<int>((u1 - 1) / ntile);
@@ -262,57 +266,63 @@ indexer_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
         const int qb = n & 1;
         const uint32_t ph = (n >> 1) & 1;
         if (!tc::mbar_wait(&sm.wempty[qb], ph ^ 1, &sm.abort)) { ok = false; break; }
-        const float w = a.w[static_cast<size_t>(b) * HH + h];
         if (!e4m3) {
-          sm.wsm[qb][h] = w;
+          sm.wsm[qb][lane] = a.w[static_cast<size_t>(b) * HH + lane];
+          sm.wsm[qb][lane + 32] = a.w[static_cast<size_t>(b) * HH + lane + 32];
           tc::mbar_arrive(&sm.pfull[qb]);
           continue;
         }
         if (!tc::mbar_wait(&sm.qfull[qb], ph, &sm.abort)) { ok = false; break; }
         if (!tc::mbar_wait(&sm.pempty[qb], ph ^ 1, &sm.abort)) { ok = false; break; }
-        float amax = 0.0f;
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          const int h = lane + 32 * hh;
+          const int sw = h & 7;
+          const float w = a.w[static_cast<size_t>(b) * HH + h];
+          float amax = 0.0f;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const uint8_t* src = sm.qs[qb][hf] + h * 128;
+          for (int hf = 0; hf < 2; ++hf) {
+            const uint8_t* src = sm.qs[qb][hf] + h * 128;
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            float f[8];
-            bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + ((j ^ sw) << 4)), f);
+            for (int j = 0; j < 8; ++j) {
+              float f[8];
+              bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + ((j ^ sw) << 4)), f);
 #pragma unroll
-            for (int t = 0; t < 8; ++t) amax = fmaxf(amax, fabsf(f[t]));
+              for (int t = 0; t < 8; ++t) amax = fmaxf(amax, fabsf(f[t]));
+            }
           }
-        }
-        // 2^e with max|q| 2^e in [128, 256); e kept where 2^e and 2^-e are normal
-        const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
-        const int e = amax > 0.0f ? max(-120, min(126, 134 - ex)) : 0;
-        const float scale = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
-        const float inv_scale = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-        uint8_t* dst_hi = sm.qsp[qb] + h * 128;
-        uint8_t* dst_lo = sm.qsp[qb] + (HH + h) * 128;
+          // 2^e with max|q| 2^e in [128, 256); e kept where 2^e and 2^-e are normal
+          const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+          const int e = amax > 0.0f ? max(-120, min(126, 134 - ex)) : 0;
+          const float scale = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+          const float inv_scale = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+          uint8_t* dst_hi = sm.qsp[qb] + h * 128;
+          uint8_t* dst_lo = sm.qsp[qb] + (HH + h) * 128;
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          // e4m3 chunk cc = features 16cc .. 16cc+15 = bf16 chunks 2(cc&3), 2(cc&3)+1 of half cc/4
-          const uint8_t* src = sm.qs[qb][cc >> 2] + h * 128;
-          const int c0 = 2 * (cc & 3);
-          float f[16];
-          bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + ((c0 ^ sw) << 4)), f);
-          bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + (((c0 + 1) ^ sw) << 4)), f + 8);
-          uint32_t hw[4], lw[4];
+          for (int cc = 0; cc < 8; ++cc) {
+            // e4m3 chunk cc = features 16cc .. 16cc+15 = bf16 chunks 2(cc&3), 2(cc&3)+1 of half cc/4
+            const uint8_t* src = sm.qs[qb][cc >> 2] + h * 128;
+            const int c0 = 2 * (cc & 3);
+            float f[16];
+            bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + ((c0 ^ sw) << 4)), f);
+            bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + (((c0 + 1) ^ sw) << 4)), f + 8);
+            uint32_t hw[4], lw[4];
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            const float x0 = f[4 * t] * scale, x1 = f[4 * t + 1] * scale;
-            const float x2 = f[4 * t + 2] * scale, x3 = f[4 * t + 3] * scale;
-            const uint32_t h01 = f32x2_to_e4m3x2(x0, x1), h23 = f32x2_to_e4m3x2(x2, x3);
-            const float2 b01 = e4m3x2_to_f32x2(h01), b23 = e4m3x2_to_f32x2(h23);
-            const uint32_t l01 = f32x2_to_e4m3x2(x0 - b01.x, x1 - b01.y);
-            const uint32_t l23 = f32x2_to_e4m3x2(x2 - b23.x, x3 - b23.y);
-            hw[t] = h01 | (h23 << 16);
-            lw[t] = l01 | (l23 << 16);
+            for (int t = 0; t < 4; ++t) {
+              const float x0 = f[4 * t] * scale, x1 = f[4 * t + 1] * scale;
+              const float x2 = f[4 * t + 2] * scale, x3 = f[4 * t + 3] * scale;
+              const uint32_t h01 = f32x2_to_e4m3x2(x0, x1), h23 = f32x2_to_e4m3x2(x2, x3);
+              const float2 b01 = e4m3x2_to_f32x2(h01), b23 = e4m3x2_to_f32x2(h23);
+              const uint32_t l01 = f32x2_to_e4m3x2(x0 - b01.x, x1 - b01.y);
+              const uint32_t l23 = f32x2_to_e4m3x2(x2 - b23.x, x3 - b23.y);
+              hw[t] = h01 | (h23 << 16);
+              lw[t] = l01 | (l23 << 16);
+            }
+            *reinterpret_cast<uint4*>(dst_hi + ((cc ^ sw) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(dst_lo + ((cc ^ sw) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
-          *reinterpret_cast<uint4*>(dst_hi + ((cc ^ sw) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(dst_lo + ((cc ^ sw) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          sm.wsm[qb][h] = w * inv_scale;
         }
-        sm.wsm[qb][h] = w * inv_scale;
         // the bf16 q buffer is released only now that its values have been
         // used, so that the next copy into it cannot overtake a load
         tc::mbar_arrive(&sm.qempty[qb]);
