@@ -20,14 +20,16 @@
 // scores, and the output accumulates in TMEM with d on the lanes.
 //
 // Persistent CTAs (one per SM) walk query rows row = blockIdx.x + i*gridDim.x.
-// Warp roles (11 warps):
+// Warp roles (12 warps):
 //   warps 0-7  softmax + epilogue in two head groups: warps 0-3 own heads
 //              0-15, warps 4-7 heads 16-31 (warp w reads TMEM lane quarter
 //              w % 4); thread = key lane for P, = d lane for O.  Thread 0
 //              also loads Q (TMA tile) and the index row (bulk copy) two
 //              rows ahead into a double buffer.
-//   warp 8     MMA issuer, over the CTA's tiles in one flat sequence:
-//              QK^T of tile g, then PV of tile g-1
+//   warp 8     MMA issuer of QK^T, over the CTA's tiles in one flat sequence
+//   warp 11    MMA issuer of PV (tile g after its P is written); two issuing
+//              threads, because the issue of a tcgen05.mma holds its thread
+//              about as long as one of these N = 32 MMAs runs
 //   warps 9-10 producers: the K rows and the V rows of every tile, gathered
 //              with 16-byte asynchronous copies into a ring of 32 KB slots
 //              (order K0 V0 K1 V1 ...) in the 128-byte-swizzled operand layout.
@@ -75,7 +77,8 @@ constexpr int PROD_WARPS = 2;
 constexpr int PROD_THREADS = PROD_WARPS * 32;
 constexpr int PROD_ROWS = KT * 16 / PROD_THREADS;   // rows of a slot each producer thread copies (one chunk each)
 constexpr int LAG = 2;                       // slots issued after a slot before it is published
-constexpr int NTHREADS = (9 + PROD_WARPS) * 32;
+constexpr int PV_WARP = PROD_WARP0 + PROD_WARPS;   // 11
+constexpr int NTHREADS = (PV_WARP + 1) * 32;
 constexpr uint32_t TMEM_COLS = 128;          // S: 2 x 32 columns, O: 2 x 32 columns
 constexpr float kTau = 8.0f;
 constexpr float kMInit = -1.0e30f;           // reference max before any valid key (finite: no inf - inf)
@@ -167,7 +170,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       tc::mbar_init(&sm.ofull[s], 1);
       tc::mbar_init(&sm.oempty[s], SOFT_THREADS);
     }
-    tc::mbar_init(&sm.drain, 1);
+    tc::mbar_init(&sm.drain, 2);            // both MMA issuers
     sm.abort = 0;
     tc::fence_mbar_init();
   }
@@ -182,7 +185,38 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   const uint32_t tS = tmem;          // columns 0..63: S buffers
   const uint32_t tO = tmem + 64;     // columns 64..127: O buffers
 
-  if (warp >= PROD_WARP0) {
+  if (warp == PV_WARP) {
+    // ================= MMA issuer: O^T += V^T P^T =================
+    if (lane == 0) {
+      bool ok = true;
+      for (uint32_t gp = 0; ok && gp < n_tiles; ++gp) {
+        const int n = static_cast<int>(gp / nt);
+        const int j = static_cast<int>(gp % nt);
+        const int ob = n & 1;
+        const int pb = gp & 1;
+        const uint32_t itv = 2 * gp + 1;
+        const int slot = static_cast<int>(itv % NSLOT);
+        if (j == 0 && !tc::mbar_wait(&sm.oempty[ob], ((n >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
+        if (!tc::mbar_wait(&sm.full[slot], (itv / NSLOT) & 1, &sm.abort)) { ok = false; break; }
+        if (!tc::mbar_wait(&sm.pfull[pb], (gp >> 1) & 1, &sm.abort)) { ok = false; break; }
+        tc::tc_fence_after();
+        const uint32_t vb = tc::smem_u32(sm.ring[slot]);
+        const uint32_t pbase = tc::smem_u32(sm.ps[pb]);
+#pragma unroll
+        for (int kk = 0; kk < KT / 16; ++kk)
+          tc::mma_f16(tO + ob * HQ, tc::sdesc(vb + kk * 2048, HALF_BYTES, 1024, 2),
+                      tc::sdesc(pbase + kk * 1024, 0, 512, 4), IDESC_PV, (j > 0 || kk != 0) ? 1u : 0u);
+        tc::mma_commit(&sm.empty[slot]);
+        tc::mma_commit(&sm.pempty[pb]);
+        if (j == nt - 1) tc::mma_commit(&sm.ofull[ob]);
+      }
+      if (!ok) set_abort(sm, status);
+      // every MMA issued so far is complete before tensor memory is released
+      tc::mma_commit(&sm.drain);
+      if (!tc::mbar_wait(&sm.drain, 0, nullptr, 4000000000ull)) set_abort(sm, status);
+    }
+    __syncwarp();
+  } else if (warp >= PROD_WARP0) {
     // ================= producers =================
     constexpr int RSTEP = PROD_THREADS / 16;
     const int pt = tid - PROD_WARP0 * 32;            // 0 .. PROD_THREADS-1
@@ -235,56 +269,30 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     for (uint32_t i = (it > LAG ? it - LAG : 0); i < it; ++i) tc::mbar_arrive(&sm.full[i % NSLOT]);
     if (!ok) set_abort(sm, status);
   } else if (warp == MMA_WARP) {
-    // ================= MMA issuer =================
+    // ================= MMA issuer: S^T = K Q^T =================
     if (lane == 0) {
       bool ok = true;
-      for (uint32_t g = 0; ok && g <= n_tiles; ++g) {
-        if (g < n_tiles) {
-          // S^T(g) = K_g Q^T
-          const int n = static_cast<int>(g / nt);
-          const int j = static_cast<int>(g % nt);
-          const int qb = n & 1;
-          const int sb = g & 1;
-          const uint32_t itk = 2 * g;
-          const int slot = static_cast<int>(itk % NSLOT);
-          if (j == 0 && !tc::mbar_wait(&sm.qfull[qb], (n >> 1) & 1, &sm.abort)) { ok = false; break; }
-          if (!tc::mbar_wait(&sm.sempty[sb], ((g >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
-          if (!tc::mbar_wait(&sm.full[slot], (itk / NSLOT) & 1, &sm.abort)) { ok = false; break; }
-          tc::tc_fence_after();
-          const uint32_t kb = tc::smem_u32(sm.ring[slot]);
-          const uint32_t q0 = tc::smem_u32(sm.qs[qb]);
+      for (uint32_t g = 0; ok && g < n_tiles; ++g) {
+        const int n = static_cast<int>(g / nt);
+        const int j = static_cast<int>(g % nt);
+        const int qb = n & 1;
+        const int sb = g & 1;
+        const uint32_t itk = 2 * g;
+        const int slot = static_cast<int>(itk % NSLOT);
+        if (j == 0 && !tc::mbar_wait(&sm.qfull[qb], (n >> 1) & 1, &sm.abort)) { ok = false; break; }
+        if (!tc::mbar_wait(&sm.sempty[sb], ((g >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
+        if (!tc::mbar_wait(&sm.full[slot], (itk / NSLOT) & 1, &sm.abort)) { ok = false; break; }
+        tc::tc_fence_after();
+        const uint32_t kb = tc::smem_u32(sm.ring[slot]);
+        const uint32_t q0 = tc::smem_u32(sm.qs[qb]);
 #pragma unroll
-          for (int kk = 0; kk < DH / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
-            const uint32_t qoff = (kk >> 2) * (Q_BYTES / 2) + (kk & 3) * 32;
-            tc::mma_f16(tS + sb * HQ, tc::sdesc_k_sw128(kb + off), tc::sdesc_k_sw128(q0 + qoff), IDESC_QK, kk != 0);
-          }
-          tc::mma_commit(&sm.empty[slot]);
-          tc::mma_commit(&sm.sfull[sb]);
+        for (int kk = 0; kk < DH / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
+          const uint32_t qoff = (kk >> 2) * (Q_BYTES / 2) + (kk & 3) * 32;
+          tc::mma_f16(tS + sb * HQ, tc::sdesc_k_sw128(kb + off), tc::sdesc_k_sw128(q0 + qoff), IDESC_QK, kk != 0);
         }
-        if (g > 0) {
-          // O^T += V_{g-1}^T P_{g-1}^T
-          const uint32_t gp = g - 1;
-          const int n = static_cast<int>(gp / nt);
-          const int j = static_cast<int>(gp % nt);
-          const int ob = n & 1;
-          const int pb = gp & 1;
-          const uint32_t itv = 2 * gp + 1;
-          const int slot = static_cast<int>(itv % NSLOT);
-          if (j == 0 && !tc::mbar_wait(&sm.oempty[ob], ((n >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
-          if (!tc::mbar_wait(&sm.full[slot], (itv / NSLOT) & 1, &sm.abort)) { ok = false; break; }
-          if (!tc::mbar_wait(&sm.pfull[pb], (gp >> 1) & 1, &sm.abort)) { ok = false; break; }
-          tc::tc_fence_after();
-          const uint32_t vb = tc::smem_u32(sm.ring[slot]);
-          const uint32_t pbase = tc::smem_u32(sm.ps[pb]);
-#pragma unroll
-          for (int kk = 0; kk < KT / 16; ++kk)
-            tc::mma_f16(tO + ob * HQ, tc::sdesc(vb + kk * 2048, HALF_BYTES, 1024, 2),
-                        tc::sdesc(pbase + kk * 1024, 0, 512, 4), IDESC_PV, (j > 0 || kk != 0) ? 1u : 0u);
-          tc::mma_commit(&sm.empty[slot]);
-          tc::mma_commit(&sm.pempty[pb]);
-          if (j == nt - 1) tc::mma_commit(&sm.ofull[ob]);
-        }
+        tc::mma_commit(&sm.empty[slot]);
+        tc::mma_commit(&sm.sfull[sb]);
       }
       if (!ok) set_abort(sm, status);
       // every MMA issued so far is complete before tensor memory is released
