@@ -2,11 +2,17 @@
 //
 // Same score as the prefill kernel (DSA lightning-indexer score used by
 // IndexCache's Full layers; notes page "NLP--IndexCache", "背景 & 问题提出"),
-// but the work is spread over the KEYS: one CTA per (tile of keys, query
-// row), so a handful of query rows still fills the GPU.  Each query row's
-// causal scores are staged in the workspace (one fp32 row per query, O(L),
-// never an L x L matrix), then one CTA per row selects the exact top-k and
-// writes the positions in ascending order.
+// but the work is spread over the KEYS, so a handful of query rows still
+// fills the GPU.  Each query row's causal scores are staged in the workspace
+// (one fp32 row per query, O(L), never an L x L matrix), then the exact
+// top-k is selected and written in ascending position order.
+//
+// Scores: the tensor-core kernel (indexer_decode_tc.cu) for one row per
+// sequence with H = 64, d = 128; otherwise decode_scores_kernel below (one
+// CTA per (tile of keys, query row), mma.sync).
+// Select: with the tensor-core scorer and a workspace that holds the
+// histogram and candidate buffers, the chunked select (select_chunk_kernel +
+// select_finish_kernel); otherwise decode_select_kernel, one CTA per row.
 #include "ic_common.cuh"
 #include "ic_kernels.h"
 #include "topk_stream.cuh"

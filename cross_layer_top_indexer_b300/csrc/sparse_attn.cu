@@ -274,20 +274,38 @@ sparse_attn_kernel(AttnArgs a, int nsplit, int chunks_per_split, float* partials
 }
 
 // Merge the splits of one (row, head): block = DH threads, grid = (rows, Hq).
+// Every split's values are loaded before the first is used, so the loads
+// overlap (one round trip instead of one per split).
+constexpr int MAX_SPLITS = (kMaxK + KC - 1) / KC;
+
 template <int DH>
 __global__ void attn_combine_kernel(const float* partials, int nsplit, int Hq, void* O) {
   const int row = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
   const size_t stride = Partial::floats(DH);
   const float* base = partials + (size_t)row * nsplit * stride;
+  float mv[MAX_SPLITS], lv[MAX_SPLITS], ov[MAX_SPLITS];
+#pragma unroll
+  for (int s = 0; s < MAX_SPLITS; ++s) {
+    if (s < nsplit) {
+      const float* p = base + s * stride;
+      mv[s] = p[h];
+      lv[s] = p[HQMAX + h];
+      ov[s] = p[2 * HQMAX + (size_t)h * DH + d];
+    }
+  }
   float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, base[s * stride + h]);
+#pragma unroll
+  for (int s = 0; s < MAX_SPLITS; ++s)
+    if (s < nsplit) M = fmaxf(M, mv[s]);
   const float Mr = M == -INFINITY ? 0.0f : M;
   float l = 0.0f, acc = 0.0f;
-  for (int s = 0; s < nsplit; ++s) {
-    const float* p = base + s * stride;
-    const float f = exp2f(p[h] - Mr);
-    l += p[HQMAX + h] * f;
-    acc += p[2 * HQMAX + (size_t)h * DH + d] * f;
+#pragma unroll
+  for (int s = 0; s < MAX_SPLITS; ++s) {
+    if (s < nsplit) {
+      const float f = exp2f(mv[s] - Mr);
+      l += lv[s] * f;
+      acc += ov[s] * f;
+    }
   }
   const float v = l > 0.0f ? acc / l : 0.0f;
   reinterpret_cast<__nv_bfloat16*>(O)[((size_t)row * Hq + h) * DH + d] = __float2bfloat16_rn(v);
@@ -308,7 +326,7 @@ cudaError_t launch_dh(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t
   const int cps = (n_chunks + nsplit - 1) / nsplit;
   nsplit = (n_chunks + cps - 1) / cps;
   const size_t need = nsplit > 1 ? (size_t)rows * nsplit * Partial::floats(DH) * sizeof(float) : 0;
-  if (need > ws_bytes) return cudaErrorInvalidValue;
+  if (need > ws_bytes || nsplit > MAX_SPLITS) return cudaErrorInvalidValue;
   const size_t smem = sizeof(AttnSmem<DH>);
   cudaError_t e = cudaFuncSetAttribute(sparse_attn_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
