@@ -283,6 +283,39 @@ def run_decode(binding, pattern, steps_tok, seed, dev, gpu_index):
         torch.cuda.synchronize()
     binding.stream_status()
     ms = t0.elapsed_time(t1)
+    clocks = clk.summary()
+    # the same 64 steps replayed from CUDA graphs (one graph per step, captured
+    # before the timed region): the kernels and the work are the same, the
+    # host launch gaps between ~140 short kernels per step are gone
+    graph = None
+    try:
+        cs = torch.cuda.Stream()
+        graphs = []
+        torch.cuda.synchronize()
+        for f in fwds:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cs):
+                f(cs)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        for g in graphs[:3]:
+            g.replay()
+        torch.cuda.synchronize()
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        with ClockSampler(gpu_index) as clk_g:
+            g0.record()
+            for g in graphs:
+                g.replay()
+            g1.record()
+            torch.cuda.synchronize()
+        binding.stream_status()
+        ms_g = g0.elapsed_time(g1)
+        graph = {"value": cfg.B * steps_tok / (ms_g * 1e-3), "unit": "tok/s", "ms_per_token_step": ms_g / steps_tok,
+                 "clocks": clk_g.summary()}
+        del graphs
+    except Exception as ex:  # capture refused: report it, the stream-launched figure stands
+        graph = {"unavailable": ("%s: %s" % (type(ex).__name__, ex))[:240]}
     # per-call breakdown at the last context length: each call alone, repeated,
     # CUDA events on the stream (a traced step would also count launch gaps)
     q_last = cfg.q_pos0 + steps_tok - 1
@@ -326,7 +359,7 @@ def run_decode(binding, pattern, steps_tok, seed, dev, gpu_index):
     return {"value": cfg.B * steps_tok / (ms * 1e-3), "unit": "tok/s", "ms_per_token_step": ms / steps_tok,
             "steps": steps_tok, "batch": cfg.B, "context": cfg.q_pos0, "pattern": pattern,
             "indexer_ms_per_F_layer": idx_layer_ms, "attn_ms_per_layer": attn_layer_ms,
-            "kernels": roof, "clocks": clk.summary()}
+            "kernels": roof, "clocks": clocks, "graph_replay": graph}
 
 
 # ---------------------------------------------------------------------------
