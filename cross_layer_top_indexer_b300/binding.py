@@ -21,7 +21,8 @@ IC_BF16, IC_E4M3 = 0, 1
 
 EXPORTED = ("ic_workspace_size", "ic_indexer_topk", "ic_sparse_attn", "ic_forward_pattern",
             "ic_forward_pattern_traced", "ic_trace_create", "ic_trace_destroy", "ic_trace_read",
-            "ic_stream_status", "ic_last_error", "ic_abi_version", "ic_indexer_topk_noalloc")
+            "ic_stream_status", "ic_last_error", "ic_abi_version", "ic_indexer_topk_noalloc",
+            "ic_overlap", "ic_greedy_full_layers", "ic_debug_set_wait_limit_ns")
 
 
 class IndexCacheError(RuntimeError):
@@ -51,6 +52,9 @@ class ICLayer(ctypes.Structure):
                 ("w", ctypes.c_void_p), ("Q", ctypes.c_void_p), ("K", ctypes.c_void_p),
                 ("V", ctypes.c_void_p), ("O", ctypes.c_void_p)]
 
+
+# double (*)(const char* pattern, void* user)
+LOSS_FN = ctypes.CFUNCTYPE(ctypes.c_double, ctypes.c_char_p, ctypes.c_void_p)
 
 _lib = None
 
@@ -89,6 +93,12 @@ def load(path: str = LIB_PATH):
     lib.ic_last_error.restype = ctypes.c_char_p
     lib.ic_abi_version.argtypes = []
     lib.ic_abi_version.restype = i
+    lib.ic_debug_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    lib.ic_debug_set_wait_limit_ns.restype = i
+    lib.ic_overlap.argtypes = [i, i, vp, vp, vp, vp, vp]
+    lib.ic_overlap.restype = i
+    lib.ic_greedy_full_layers.argtypes = [i, i, LOSS_FN, vp, ctypes.c_char_p, ctypes.POINTER(ctypes.c_longlong)]
+    lib.ic_greedy_full_layers.restype = i
     _lib = lib
     return lib
 
@@ -311,6 +321,48 @@ def forward_pattern(pattern: str, layers: Sequence[dict], k: int, q_pos0: int = 
                                   _stream(stream))
     _raise(code)
     return index_cache, calls.value
+
+
+def overlap(idx_a: torch.Tensor, idx_b: torch.Tensor, k: Optional[int] = None, counts: bool = False,
+            stream=None):
+    """ic_overlap: per-row |I_a ∩ I_b| / k of two index tensors [..., k] int32.
+
+    Returns the fp32 ratios (shape of the leading axes), and the int32 counts
+    too when ``counts`` is true."""
+    lib = load()
+    if idx_a.shape != idx_b.shape or idx_a.dtype != torch.int32 or idx_b.dtype != torch.int32:
+        raise ValueError("idx_a and idx_b must be int32 tensors of one shape")
+    k = idx_a.shape[-1] if k is None else k
+    R = idx_a.numel() // idx_a.shape[-1]
+    ratio = torch.empty(idx_a.shape[:-1], dtype=torch.float32, device=idx_a.device)
+    cnt = torch.empty(idx_a.shape[:-1], dtype=torch.int32, device=idx_a.device) if counts else None
+    _raise(lib.ic_overlap(R, k, _ptr(idx_a), _ptr(idx_b), _ptr(ratio), _ptr(cnt), _stream(stream)))
+    return (ratio, cnt) if counts else ratio
+
+
+def greedy_full_layers(n_layers: int, removals: int, evaluate_loss) -> tuple:
+    """ic_greedy_full_layers with a Python loss: ``evaluate_loss(pattern: str)
+    -> float`` runs the caller's model under the pattern.  Returns (pattern,
+    number of loss evaluations).  An exception in the loss stops the search
+    and is re-raised."""
+    lib = load()
+    failure = []
+
+    def cb(pat, _user):
+        try:
+            return float(evaluate_loss(pat.decode()))
+        except BaseException as ex:  # reported after the C call returns
+            failure.append(ex)
+            return float("nan")
+
+    fn = LOSS_FN(cb)
+    out = ctypes.create_string_buffer(max(n_layers, 0) + 1)
+    fw = ctypes.c_longlong(0)
+    code = lib.ic_greedy_full_layers(int(n_layers), int(removals), fn, None, out, ctypes.byref(fw))
+    if failure:
+        raise failure[0]
+    _raise(code)
+    return out.value.decode(), fw.value
 
 
 def stream_status(stream=None) -> None:

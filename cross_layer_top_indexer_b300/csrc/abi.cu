@@ -13,6 +13,7 @@
 
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -51,6 +52,10 @@ int* device_status_ptr() {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Limit of the tensor-core prefill indexer's waits on other roles; 0 means
+// the default (ic::kWaitLimitNs).  Set only through ic_debug_set_wait_limit_ns.
+std::atomic<uint64_t> g_wait_ns{0};
 
 }  // namespace
 
@@ -97,6 +102,18 @@ ic_status check_attn(int B, int T, int S, int S_cap, int Hq, int Dh, int k, cons
   return IC_OK;
 }
 
+}  // namespace
+
+namespace ic {
+// Argument checks of ic_indexer_topk, shared with the other indexer entry points.
+ic_status check_indexer_args(int B, int T, int S, int S_cap, int H, int D, int k, int q_pos0, const void* q,
+                             const void* kI, int k_dtype, const float* k_scale, const float* w, const void* idx) {
+  return check_indexer(B, T, S, S_cap, H, D, k, q_pos0, q, kI, k_dtype, k_scale, w, idx);
+}
+}  // namespace ic
+
+namespace {
+
 size_t indexer_ws(int B, int T, int S) {
   return T <= ic::kDecodeMaxT ? ic::indexer_decode_ws_fast_bytes(B, T, S) : 0;
 }
@@ -105,8 +122,9 @@ ic_status cuda_fail(cudaError_t e, const char* what) {
   return fail(IC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-ic_status run_indexer(const ic::IndexerArgs& a, void* ws, size_t ws_bytes, cudaStream_t st) {
+ic_status run_indexer(ic::IndexerArgs a, void* ws, size_t ws_bytes, cudaStream_t st) {
   int* status = device_status_ptr();
+  a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
   cudaError_t e;
   if (a.T <= ic::kDecodeMaxT) {
     const size_t need = ic::indexer_decode_ws_bytes(a.B, a.T, a.S);
@@ -316,6 +334,24 @@ IC_EXPORT ic_status ic_trace_read(ic_trace* t, int* n_forwards, float* indexer_m
   if (n_forwards) *n_forwards = t->used;
   t->used = 0;
   t->roles.clear();
+  return IC_OK;
+}
+
+IC_EXPORT ic_status ic_overlap(int R, int k, const int32_t* idx_a, const int32_t* idx_b, float* ratio_out,
+                               int32_t* count_out, void* stream) {
+  g_msg[0] = 0;
+  if (R < 1 || k < 1) return fail(IC_ERR_ARG, "sizes must be positive (R=%d k=%d)", R, k);
+  if (!idx_a || !idx_b || !ratio_out) return fail(IC_ERR_ARG, "null tensor pointer");
+  if (!aligned16(idx_a) || !aligned16(idx_b) || !aligned16(ratio_out) || (count_out && !aligned16(count_out)))
+    return fail(IC_ERR_ARG, "tensor pointers must be 16-byte aligned");
+  if (k > ic::kMaxK) return fail(IC_ERR_UNSUPPORTED, "k=%d: at most %d", k, ic::kMaxK);
+  cudaError_t e = ic::launch_overlap(R, k, idx_a, idx_b, ratio_out, count_out, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? IC_OK : cuda_fail(e, "overlap launch");
+}
+
+IC_EXPORT ic_status ic_debug_set_wait_limit_ns(unsigned long long ns) {
+  g_msg[0] = 0;
+  g_wait_ns.store(static_cast<uint64_t>(ns), std::memory_order_relaxed);
   return IC_OK;
 }
 

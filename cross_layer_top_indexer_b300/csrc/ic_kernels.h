@@ -7,6 +7,9 @@
 
 namespace ic {
 
+// Default limit of a bounded device wait on another role's progress.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
 struct IndexerArgs {
   const void* q;         // [B,T,H,D] bf16
   const void* kI;        // [B,S_cap,D] bf16 or e4m3
@@ -14,6 +17,7 @@ struct IndexerArgs {
   const float* w;        // [B,T,H]
   int32_t* idx;          // [B,T,k]
   int B, T, S, S_cap, H, D, k, q_pos0, e4m3;
+  uint64_t wait_ns = 0;  // limit of the tensor-core prefill kernel's waits; 0 = kWaitLimitNs
 };
 
 struct AttnArgs {
@@ -64,6 +68,10 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, void* ws, size_t ws_bytes, int
 bool sparse_attn_tc_supported(const AttnArgs& a);
 cudaError_t launch_sparse_attn_tc(const AttnArgs& a, int* dev_status, cudaStream_t st);
 
+// Per-row overlap |I_a ∩ I_b| / k of two index tensors [R, k] (count optional).
+cudaError_t launch_overlap(int R, int k, const int32_t* ia, const int32_t* ib, float* ratio, int32_t* count,
+                           cudaStream_t st);
+
 }  // namespace ic
 
 #include "../../include/indexcache.h"
@@ -71,6 +79,9 @@ cudaError_t launch_sparse_attn_tc(const AttnArgs& a, int* dev_status, cudaStream
 namespace ic {
 // Shared by the entry points of the library (defined in abi.cu).
 ic_status report_error(ic_status st, const char* msg);
+// The argument checks of ic_indexer_topk (message set on failure).
+ic_status check_indexer_args(int B, int T, int S, int S_cap, int H, int D, int k, int q_pos0, const void* q,
+                             const void* kI, int k_dtype, const float* k_scale, const float* w, const void* idx);
 void clear_error();
 int* device_status();
 }  // namespace ic

@@ -142,6 +142,9 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // limit of every wait on another role's progress (the wind-down waits for
+  // this CTA's own copies and MMAs keep their fixed limits)
+  const uint64_t lim = a.wait_ns ? a.wait_ns : kWaitLimitNs;
   const int g = n_groups - 1 - static_cast<int>(blockIdx.x);   // longest causal range first
   const int b = blockIdx.y;
   const int t0 = g * QPB;
@@ -200,7 +203,7 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
       for (int it = 0; !E4M3 && it < 2 * nt; ++it) {
         const int s = it % KSTAGES;
         const uint32_t ph = (it / KSTAGES) & 1;
-        if (!tc::mbar_wait(&sm.empty[s], ph ^ 1, &sm.abort)) { set_abort(sm, status); break; }
+        if (!tc::mbar_wait(&sm.empty[s], ph ^ 1, &sm.abort, lim)) { set_abort(sm, status); break; }
         tc::mbar_arrive_expect_tx(&sm.full[s], KT * 128);
         tc::tma_load_2d(sm.kst[s], &tm_k, &sm.full[s], (it & 1) * 64, krow0 + (it >> 1) * KT);
         issued = it + 1;
@@ -214,19 +217,19 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
   } else if (warp == 1) {
     // ================= MMA issuer =================
     if (lane == 0) {
-      bool ok = tc::mbar_wait(E4M3 ? &sm.qconv : &sm.qfull, 0, &sm.abort);
+      bool ok = tc::mbar_wait(E4M3 ? &sm.qconv : &sm.qfull, 0, &sm.abort, lim);
       if (!ok) set_abort(sm, status);
       const uint32_t qb0 = tc::smem_u32(sm.qb[0]);
       const uint32_t qb1 = tc::smem_u32(sm.qb[1]);
       for (int j = 0; ok && j < nt; ++j) {
         const int acc = j & 1;
-        if (!tc::mbar_wait(&sm.tempty[acc], ((j >> 1) & 1) ^ 1, &sm.abort)) { set_abort(sm, status); break; }
+        if (!tc::mbar_wait(&sm.tempty[acc], ((j >> 1) & 1) ^ 1, &sm.abort, lim)) { set_abort(sm, status); break; }
         tc::tc_fence_after();
         const uint32_t d_tmem = tmem + acc * NCOL;
         for (int h = 0; h < 2; ++h) {
           const int it = 2 * j + h;
           const int s = it % KSTAGES;
-          if (!tc::mbar_wait(&sm.full[s], (it / KSTAGES) & 1, &sm.abort)) { set_abort(sm, status); ok = false; break; }
+          if (!tc::mbar_wait(&sm.full[s], (it / KSTAGES) & 1, &sm.abort, lim)) { set_abort(sm, status); ok = false; break; }
           tc::tc_fence_after();
           const uint32_t a_base = tc::smem_u32(sm.kst[s]);
           const uint32_t b_base = h ? qb1 : qb0;
@@ -266,8 +269,8 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
       auto store_tile = [&](int j, const uint4 (&raw)[16]) -> bool {
         const int it0 = 2 * j;
         const int s0 = it0 % KSTAGES, s1 = (it0 + 1) % KSTAGES;
-        if (!tc::mbar_wait(&sm.empty[s0], ((it0 / KSTAGES) & 1) ^ 1, &sm.abort)) return false;
-        if (!tc::mbar_wait(&sm.empty[s1], (((it0 + 1) / KSTAGES) & 1) ^ 1, &sm.abort)) return false;
+        if (!tc::mbar_wait(&sm.empty[s0], ((it0 / KSTAGES) & 1) ^ 1, &sm.abort, lim)) return false;
+        if (!tc::mbar_wait(&sm.empty[s1], (((it0 + 1) / KSTAGES) & 1) ^ 1, &sm.abort, lim)) return false;
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           const int c = ct + 64 * u;
@@ -318,7 +321,7 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
 
     if constexpr (E4M3) {
       // this warpgroup's two q rows: thread = (row q0 + wtid / 64, head wtid % 64)
-      const bool okq = tc::mbar_wait(&sm.qfull, 0, &sm.abort);
+      const bool okq = tc::mbar_wait(&sm.qfull, 0, &sm.abort, lim);
       if (!okq) set_abort(sm, status);
       const int qi = q0 + (wtid >> 6), hd = wtid & 63;
       const int qr = qi * HH + hd;                  // row of the 256-row B operand
@@ -369,7 +372,7 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
         const int sn = (j + 1) * KT + key_local;
         ks_next = sn < n_keys ? __ldg(ksrow + sn) : 1.0f;
       }
-      const bool ok = tc::mbar_wait(&sm.tfull[acc], (j >> 1) & 1, &sm.abort);
+      const bool ok = tc::mbar_wait(&sm.tfull[acc], (j >> 1) & 1, &sm.abort, lim);
       if (!ok) set_abort(sm, status);
       tc::tc_fence_after();
       uint32_t key[2];

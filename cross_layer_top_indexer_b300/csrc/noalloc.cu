@@ -30,28 +30,29 @@ constexpr size_t kScratchBytes = 32ull << 20;   // 32 MiB: 32 rows of 262144 sco
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 // In host code `g_noalloc_scratch` names a host-side stand-in, not device
-// memory: its device address is looked up once per device, with that device
-// current, and passed to the kernels.
+// memory: its device address is looked up per device, with that device
+// current, and passed to the kernels.  Only a successful lookup is kept, so
+// a failed first attempt (for instance one made during a stream capture) is
+// retried by the next call.
 constexpr int kMaxDevices = 64;
 void* g_scratch_addr[kMaxDevices];
-cudaError_t g_scratch_err[kMaxDevices];
-std::once_flag g_scratch_once[kMaxDevices];
+std::mutex g_scratch_mu;
 
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::call_once(g_scratch_once[dev], [dev] {
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
     void* p = nullptr;
-    g_scratch_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p) return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
     g_scratch_addr[dev] = p;
-  });
+  }
   *out = g_scratch_addr[dev];
-  return g_scratch_err[dev];
+  return cudaSuccess;
 }
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 ic_status bad(ic_status st, const char* fmt, long long a = 0, long long b = 0) {
   char buf[256];
@@ -66,19 +67,10 @@ extern "C" __attribute__((visibility("default"))) ic_status ic_indexer_topk_noal
     const float* k_scale, const float* w, int32_t* idx_out, void* stream) {
   ic::clear_error();
   if (S_cap == 0) S_cap = S;
-  if (B < 1 || T < 1 || S < 1 || H < 1 || D < 1 || k < 1 || q_pos0 < 0)
-    return bad(IC_ERR_ARG, "sizes must be positive");
-  if ((long long)q_pos0 + T > S) return bad(IC_ERR_ARG, "q_pos0 + T (%lld) exceeds S (%lld)", (long long)q_pos0 + T, S);
-  if (S_cap < S) return bad(IC_ERR_ARG, "S_cap (%lld) is smaller than S (%lld)", S_cap, S);
-  if (k_dtype != IC_BF16 && k_dtype != IC_E4M3) return bad(IC_ERR_ARG, "k_dtype %lld unknown", k_dtype);
-  if (!q || !kI || !w || !idx_out) return bad(IC_ERR_ARG, "null tensor pointer");
-  if ((k_dtype == IC_E4M3) != (k_scale != nullptr))
-    return bad(IC_ERR_ARG, "k_scale must be given for e4m3 keys and only for them");
-  if (!aligned16(q) || !aligned16(kI) || !aligned16(w) || !aligned16(idx_out) || (k_scale && !aligned16(k_scale)))
-    return bad(IC_ERR_ARG, "tensor pointers must be 16-byte aligned");
-  if (H > 64) return bad(IC_ERR_UNSUPPORTED, "H=%lld: at most 64 indexer heads", H);
-  if (D != 32 && D != 64 && D != 128) return bad(IC_ERR_UNSUPPORTED, "D=%lld: indexer dim must be 32, 64 or 128", D);
-  if (k > ic::kMaxK) return bad(IC_ERR_UNSUPPORTED, "k=%lld: at most %lld", k, ic::kMaxK);
+  // the checks of ic_indexer_topk, then this entry point's own limits
+  const ic_status st =
+      ic::check_indexer_args(B, T, S, S_cap, H, D, k, q_pos0, q, kI, k_dtype, k_scale, w, idx_out);
+  if (st != IC_OK) return st;
   if (T > ic::kDecodeMaxT)
     return bad(IC_ERR_UNSUPPORTED, "T=%lld: this entry point serves at most %lld query rows per sequence", T,
                ic::kDecodeMaxT);

@@ -139,9 +139,10 @@ ic_status ic_sparse_attn(int B, int T, int S, int S_cap, int Hq, int Dh, int k,
  * array inside the library (held by every GPU that loads it, until exit):
  * B * T * S * 4 bytes (S rounded up to a multiple of 4) must fit, or the call
  * returns IC_ERR_UNSUPPORTED; T > 8 also returns IC_ERR_UNSUPPORTED.  The
- * first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any
- * stream capture.  All calls share the array: calls whose kernels may
+ * first successful call on a device looks up the array's device address,
+ * with that device current, and keeps it (a failed lookup is retried by the
+ * next call); make that first call before any stream capture.  All calls
+ * share the array: calls whose kernels may
  * overlap on the GPU race on it and must be ordered by the caller.  Nothing
  * in it needs to start at zero.  Arguments, results and other errors as for
  * ic_indexer_topk. */
@@ -184,10 +185,57 @@ ic_status ic_forward_pattern_traced(const char* pattern, int n_layers, const ic_
  * *n_forwards = how many forwards were summed, and empties the trace. */
 ic_status ic_trace_read(ic_trace* trace, int* n_forwards, float* indexer_ms, float* attn_ms);
 
+/* Cross-layer overlap of two index tensors (deep-read page,
+ * "相邻层重叠很高，但“重叠率”不是搜索目标": Overlap(l, j) = |I_l ∩ I_j| / k;
+ * the page's measurement order, "一个实用的测量顺序", records it per layer):
+ *
+ *   ratio_out[r] = |A_r ∩ B_r| / k,   count_out[r] = |A_r ∩ B_r|
+ *
+ * where A_r and B_r are the sets of valid (>= 0) positions in row r of
+ * idx_a and idx_b ([R, k] int32, device).  Empty (-1) slots and repeated
+ * positions count at most once; the order within a row does not matter.
+ * ratio_out [R] fp32 (device, required); count_out [R] int32 (device, may be
+ * NULL).  Asynchronous on `stream`; no workspace.
+ * Errors: IC_ERR_ARG (sizes < 1, null or misaligned pointers),
+ * IC_ERR_UNSUPPORTED (k > 2048), IC_ERR_CUDA. */
+ic_status ic_overlap(int R, int k, const int32_t* idx_a, const int32_t* idx_b, float* ratio_out,
+                     int32_t* count_out, void* stream);
+
+/* Loss of the model under an F/S pattern: `pattern` is a NUL-terminated
+ * string of n_layers characters 'F'/'S'; `user` is passed through.  Return
+ * NaN to stop the search with an error. */
+typedef double (*ic_loss_fn)(const char* pattern, void* user);
+
+/* Training-free greedy layer selection (notes page, "核心算法：Greedy Layer
+ * Selection"; deep-read page, "Training-free：直接用语言模型损失选择 Full 层").
+ * Starts from all-F; layer 0 is never removed.  Each of `removals` rounds
+ * calls evaluate_loss on every pattern that turns one remaining F layer
+ * (other than layer 0) into S, in ascending layer order, and commits the flip
+ * with the lowest loss (ties: the lower layer).  Host code only: the loss
+ * callback runs the caller's model.  Writes the final pattern (n_layers
+ * characters + NUL) to the HOST buffer pattern_out and the number of loss
+ * evaluations, K(N-1) - K(K-1)/2, to *forwards_out (may be NULL).
+ * Errors: IC_ERR_ARG (n_layers < 1, removals outside [0, n_layers-1], null
+ * callback or output, or a NaN loss; pattern_out then holds the flips
+ * committed so far). */
+ic_status ic_greedy_full_layers(int n_layers, int removals, ic_loss_fn evaluate_loss, void* user,
+                                char* pattern_out, long long* forwards_out);
+
 /* Waits for `stream`, then reports and clears the device error word that
  * bounded waits inside the kernels set when they give up
  * (IC_ERR_DEVICE_TIMEOUT), or IC_ERR_CUDA for a failed stream. */
 ic_status ic_stream_status(void* stream);
+
+/* Debugging aid, off by default: sets the limit, in nanoseconds of device
+ * time, of every wait that the tensor-core prefill indexer (the kernel behind
+ * ic_indexer_topk for H = 64, D = 128 and more than 8 query rows) makes on
+ * another part of the same kernel; 0 restores the default (2 s).  A wait that
+ * runs out makes the kernel wind down cleanly (no trap, no hang): its copies
+ * and tensor-core work already issued are waited for, its tensor memory is
+ * released, the index rows it owns are left unspecified, and the next
+ * ic_stream_status returns IC_ERR_DEVICE_TIMEOUT.  Only a test of that path
+ * has a reason to set a small limit.  Process-wide; affects later launches. */
+ic_status ic_debug_set_wait_limit_ns(unsigned long long ns);
 
 /* Message of the calling thread's last failed call ("" if none). */
 const char* ic_last_error(void);

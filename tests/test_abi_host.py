@@ -135,3 +135,40 @@ def test_forward_workspace_too_small_is_refused(lib):
     calls = ctypes.c_int(0)
     r = lib.ic_forward_pattern(b"F", 1, arr, ctypes.byref(d), _fake(8), ctypes.byref(calls), None, 0, None)
     assert r == B.IC_ERR_ARG and "workspace" in lib.ic_last_error().decode()
+
+
+def test_overlap_argument_checks(lib):
+    f = _fake
+    assert lib.ic_overlap(0, 16, f(1), f(2), f(3), None, None) == B.IC_ERR_ARG
+    assert lib.ic_overlap(4, 0, f(1), f(2), f(3), None, None) == B.IC_ERR_ARG
+    assert lib.ic_overlap(4, 16, None, f(2), f(3), None, None) == B.IC_ERR_ARG
+    assert lib.ic_overlap(4, 16, f(1), f(2), None, None, None) == B.IC_ERR_ARG
+    assert lib.ic_overlap(4, 16, f(1) + 4, f(2), f(3), None, None) == B.IC_ERR_ARG
+    assert lib.ic_overlap(4, 4096, f(1), f(2), f(3), None, None) == B.IC_ERR_UNSUPPORTED
+
+
+def test_debug_wait_limit_setter(lib):
+    assert lib.ic_debug_set_wait_limit_ns(5) == B.IC_OK
+    assert lib.ic_debug_set_wait_limit_ns(0) == B.IC_OK
+
+
+@pytest.mark.parametrize("kw,code,text", [
+    (dict(T=9), B.IC_ERR_UNSUPPORTED, "query rows"),
+    (dict(B=32, S=300000, S_cap=300000, q_pos0=299999), B.IC_ERR_UNSUPPORTED, "scratch"),
+    (dict(kdtype=B.IC_E4M3), B.IC_ERR_ARG, "k_scale"),
+    (dict(scale=True), B.IC_ERR_ARG, "k_scale"),            # a scale given for bf16 keys
+    (dict(nullq=True), B.IC_ERR_ARG, "null"),
+    (dict(H=65), B.IC_ERR_UNSUPPORTED, "heads"),
+    (dict(S_cap=1 << 30, B=2048), B.IC_ERR_UNSUPPORTED, "too large"),
+])
+def test_noalloc_argument_checks(lib, kw, code, text):
+    # the allocation-free entry point refuses before touching any pointer
+    a = dict(B=2, T=1, S=1000, S_cap=1000, H=64, D=128, k=64, q_pos0=999, kdtype=B.IC_BF16, scale=False,
+             nullq=False)
+    a.update(kw)
+    r = lib.ic_indexer_topk_noalloc(a["B"], a["T"], a["S"], a["S_cap"], a["H"], a["D"], a["k"],
+                                    a["S"] - a["T"] if "q_pos0" not in kw else a["q_pos0"],
+                                    None if a["nullq"] else _fake(1), _fake(2), a["kdtype"],
+                                    _fake(5) if a["scale"] else None, _fake(3), _fake(4), None)
+    assert r == code, lib.ic_last_error()
+    assert text.encode() in lib.ic_last_error()
