@@ -208,10 +208,30 @@ def kernel_roofline(per, pattern, cfg, peaks, steps):
     return out
 
 
+def adjacent_overlap(binding, layers, cfg):
+    """Top-k overlap of adjacent layers in the all-F stack (deep-read page,
+    "相邻层重叠很高…": Overlap(l, l-1) = |I_l ∩ I_(l-1)| / k, averaged over the
+    query rows), through ic_indexer_topk and ic_overlap.  The synthetic layers
+    are independent draws, so the expected overlap is that of unrelated
+    top-k sets (about k / L per row on long rows), far below the pages' 0.7-1.0
+    for a trained model; the figure checks the measurement path."""
+    bufs = [torch.empty((cfg.B, cfg.T, cfg.k), dtype=torch.int32, device=layers[0]["Q"].device) for _ in range(2)]
+    out = []
+    for l, L in enumerate(layers):
+        binding.indexer_topk(L["q"], L["kI"], L["w"], cfg.k, kscale=L.get("kscale"), idx_out=bufs[l & 1])
+        if l:
+            out.append(float(binding.overlap(bufs[l & 1], bufs[(l - 1) & 1]).mean().item()))
+    binding.stream_status()
+    return {"mean": statistics.mean(out), "min": min(out), "max": max(out), "per_pair": out}
+
+
 def run_e2e(binding, layers, cfg, pattern, steps, warmup):
-    """Same metric through the public API with HOST buffers: every step copies
-    each layer's inputs host->device (pinned), runs the forward, and reads
-    every layer's output back to host."""
+    """Same metric through the public per-layer API with HOST buffers.  Every
+    step copies each layer's inputs from pinned host memory (q_I/k_I/w on F
+    layers; Q/K/V on all layers), runs the layer (ic_indexer_topk on F layers,
+    ic_sparse_attn on all), and reads every layer's O back.  Uploads run on
+    one copy stream, downloads on another, the layers on the compute stream;
+    events order them, so layer l+1's uploads overlap layer l's compute."""
     dev = layers[0]["Q"].device
     kinds = ["q", "kI", "w", "Q", "K", "V"]
     host = {}
@@ -219,83 +239,152 @@ def run_e2e(binding, layers, cfg, pattern, steps, warmup):
         src = next(L[kd] for L in layers if L.get(kd) is not None)
         host[kd] = torch.empty(src.shape, dtype=src.dtype, pin_memory=True)
         host[kd].copy_(src.cpu())
-    o_host = torch.empty(layers[0]["Q"].shape, dtype=torch.bfloat16, pin_memory=True)
-    fwd = binding.Forward(pattern, layers, cfg.k, cfg.q_pos0, cfg.S)
-    stream = torch.cuda.current_stream()
-    h2d = d2h = 0
+    n = len(layers)
+    o_host = [torch.empty(layers[0]["Q"].shape, dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
+    comp = torch.cuda.current_stream()
+    up = torch.cuda.Stream()
+    down = torch.cuda.Stream()
+    up_done = [torch.cuda.Event() for _ in range(n)]
+    comp_done = [torch.cuda.Event() for _ in range(n)]
+    for e in comp_done:
+        e.record(comp)
+    cache = torch.empty((cfg.B, cfg.T, cfg.k), dtype=torch.int32, device=dev)
+    counts = {"h2d": 0, "d2h": 0}
 
     def step():
-        nonlocal h2d, d2h
-        h2d = d2h = 0
+        counts["h2d"] = counts["d2h"] = 0
         for l, L in enumerate(layers):
-            for kd in kinds:
-                if L.get(kd) is not None and (kd not in ("q", "kI", "w") or pattern[l] == "F"):
-                    L[kd].copy_(host[kd], non_blocking=True)
-                    h2d += L[kd].numel() * L[kd].element_size()
-        fwd(stream)
-        for L in layers:
-            o_host.copy_(L["O"], non_blocking=True)
-            d2h += L["O"].numel() * L["O"].element_size()
+            up.wait_event(comp_done[l])          # the previous step is done with this layer's buffers
+            with torch.cuda.stream(up):
+                for kd in kinds:
+                    if L.get(kd) is not None and (kd not in ("q", "kI", "w") or pattern[l] == "F"):
+                        L[kd].copy_(host[kd], non_blocking=True)
+                        counts["h2d"] += L[kd].numel() * L[kd].element_size()
+            up_done[l].record(up)
+        for l, L in enumerate(layers):
+            comp.wait_event(up_done[l])
+            if pattern[l] == "F":
+                binding.indexer_topk(L["q"], L["kI"], L["w"], cfg.k, kscale=L.get("kscale"), idx_out=cache,
+                                     stream=comp)
+            binding.sparse_attn(L["Q"], L["K"], L["V"], cache, O=L["O"], stream=comp)
+            comp_done[l].record(comp)
+            down.wait_event(comp_done[l])
+            with torch.cuda.stream(down):
+                o_host[l & 1].copy_(L["O"], non_blocking=True)
+            counts["d2h"] += L["O"].numel() * L["O"].element_size()
 
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
+    t0.record(comp)
+    up.wait_event(t0)
     for _ in range(steps):
         step()
-    t1.record(stream)
+    comp.wait_stream(down)
+    comp.wait_stream(up)
+    t1.record(comp)
     torch.cuda.synchronize()
     binding.stream_status()
     ms = t0.elapsed_time(t1) / steps
     del host, o_host
     return {"value": cfg.B * cfg.T / (ms * 1e-3), "unit": "tok/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps, "warmup": warmup}
+            "h2d_bytes_per_step": counts["h2d"], "d2h_bytes_per_step": counts["d2h"], "steps": steps,
+            "warmup": warmup, "api": "ic_indexer_topk / ic_sparse_attn per layer, host pinned buffers",
+            "overlap": "uploads and downloads on their own streams, ordered by events"}
+
+
+def graph_time_ms(fn, reps, stream):
+    """Device time of one call of ``fn`` (launches on ``stream``): ``reps``
+    calls captured in one CUDA graph, replayed, timed with CUDA events, so
+    host launch gaps do not count."""
+    fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(reps):
+            fn()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    del g
+    return a.elapsed_time(b) / reps
 
 
 def run_decode(binding, pattern, steps_tok, seed, dev, gpu_index):
     """The decode workload: 32 sequences with 131072 cached tokens, one new
-    query per sequence per step; step i sees S = 131073 + i keys."""
+    token per sequence per step.  Step i appends the new token's indexer key
+    (Full layers) and K/V rows at position 131072 + i of every layer
+    (ic_decode_append, one launch), then runs the stack for the query at
+    that position over S = 131073 + i keys (ic_forward_pattern)."""
     cfg = synth.DECODE.with_(pattern=pattern)
     S_cap = cfg.q_pos0 + cfg.steps
     torch.cuda.synchronize()
     layers = synth.make_stack(cfg, seed, dev, T=1, S=S_cap, indexer_layers="pattern")
     for L in layers:
         L["O"] = torch.empty_like(L["Q"])
+    # the new tokens' rows of every step, drawn before the timed region
+    new_rows = []
+    for i in range(steps_tok):
+        rows = []
+        for l, c in enumerate(pattern):
+            R = {}
+            if c == "F":
+                _, kI1, ks1, _ = synth.make_indexer_inputs(cfg, l, seed + 7 + 1000003 * (i + 1), dev, T=1, S=1)
+                R["kI"] = kI1[:, 0].contiguous()
+                R["kscale"] = ks1[:, 0].contiguous() if ks1 is not None else None
+            _, K1, V1 = synth.make_attn_inputs(cfg, l, seed + 7 + 1000003 * (i + 1), dev, T=1, S=1)
+            R["K"], R["V"] = K1[:, 0].contiguous(), V1[:, 0].contiguous()
+            rows.append(R)
+        new_rows.append(rows)
+    kd = binding.IC_E4M3 if cfg.k_dtype == "e4m3" else binding.IC_BF16
+    appends = [binding.DecodeAppend(pattern, layers, new_rows[i], kd) for i in range(steps_tok)]
     ws_need = binding.workspace_size(binding.make_dims(cfg.B, 1, S_cap, cfg.H, cfg.D, cfg.k, cfg.Hq, cfg.Dh,
-                                                       S_cap - 1, binding.IC_E4M3, S_cap))
+                                                       S_cap - 1, kd, S_cap))
     ws = torch.empty(max(ws_need, 1), dtype=torch.uint8, device=dev)
     cache = torch.empty((cfg.B, 1, cfg.k), dtype=torch.int32, device=dev)
     fwds = [binding.Forward(pattern, layers, cfg.k, cfg.q_pos0 + i, cfg.q_pos0 + i + 1, index_cache=cache, ws=ws)
             for i in range(steps_tok)]
     stream = torch.cuda.current_stream()
-    for f in fwds[:3]:
-        f(stream)
+
+    def step(i, st):
+        appends[i](cfg.q_pos0 + i, stream=st)
+        fwds[i](st)
+
+    for i in range(3):
+        step(i, stream)
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(gpu_index) as clk:
         t0.record(stream)
-        for f in fwds:
-            f(stream)
+        for i in range(steps_tok):
+            step(i, stream)
         t1.record(stream)
         torch.cuda.synchronize()
     binding.stream_status()
     ms = t0.elapsed_time(t1)
     clocks = clk.summary()
-    # the same 64 steps replayed from CUDA graphs (one graph per step, captured
-    # before the timed region): the kernels and the work are the same, the
-    # host launch gaps between ~140 short kernels per step are gone
+    # the same 64 steps replayed from CUDA graphs (one graph per step,
+    # captured before the timed region): same kernels and work, without the
+    # host launch gaps between the short kernels of a step
     graph = None
     try:
         cs = torch.cuda.Stream()
         graphs = []
         torch.cuda.synchronize()
-        for f in fwds:
+        for i in range(steps_tok):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=cs):
-                f(cs)
+                step(i, cs)
             graphs.append(g)
         torch.cuda.synchronize()
         for g in graphs[:3]:
@@ -316,32 +405,19 @@ def run_decode(binding, pattern, steps_tok, seed, dev, gpu_index):
         del graphs
     except Exception as ex:  # capture refused: report it, the stream-launched figure stands
         graph = {"unavailable": ("%s: %s" % (type(ex).__name__, ex))[:240]}
-    # per-call breakdown at the last context length: each call alone, repeated,
-    # CUDA events on the stream (a traced step would also count launch gaps)
+    # per-call device times at the last context, each call alone, measured
+    # from CUDA-graph replays of repeated calls (no host launch gaps)
     q_last = cfg.q_pos0 + steps_tok - 1
     L0 = layers[0]
-
-    def call_ms(fn, reps):
-        fn()
-        torch.cuda.synchronize()
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(reps):
-            fn()
-        b.record(stream)
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / reps
-
-    idx_layer_ms = call_ms(lambda: binding.indexer_topk(L0["q"], L0["kI"], L0["w"], cfg.k, q_last,
-                                                        kscale=L0["kscale"], S=q_last + 1, idx_out=cache, ws=ws,
-                                                        stream=stream), 10)
-    # one attention call (~25 us of device time) is shorter than its launch from
-    # Python, so its share is derived from the step: the step time less the
-    # indexer calls, over the layers
-    attn_layer_ms = max(0.0, ms / steps_tok - pattern.count("F") * idx_layer_ms) / len(pattern)
+    cs = torch.cuda.Stream()
+    idx_layer_ms = graph_time_ms(lambda: binding.indexer_topk(L0["q"], L0["kI"], L0["w"], cfg.k, q_last,
+                                                              kscale=L0["kscale"], S=q_last + 1, idx_out=cache,
+                                                              ws=ws, stream=cs), 10, cs)
+    attn_layer_ms = graph_time_ms(lambda: binding.sparse_attn(L0["Q"], L0["K"], L0["V"], cache, S=q_last + 1,
+                                                              O=L0["O"], ws=ws, stream=cs), 20, cs)
+    append_ms = graph_time_ms(lambda: appends[-1](q_last, stream=cs), 20, cs)
     binding.stream_status()
-    del layers, fwds, ws
+    del layers, fwds, ws, appends, new_rows
     torch.cuda.empty_cache()
     # algorithmic HBM bytes of one layer at the traced context S = S_cap:
     # indexer: every cached key once (d_I e4m3 bytes + its fp32 scale) plus q, w
@@ -355,11 +431,100 @@ def run_decode(binding, pattern, steps_tok, seed, dev, gpu_index):
         if t_ms > 0:
             ach = nbytes / (t_ms * 1e-3) / 1e9
             roof[name] = {"bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
-                          "bytes_per_launch": nbytes, "launch_ms": t_ms}
+                          "bytes_per_launch": nbytes, "launch_ms": t_ms, "timing": "CUDA-graph replay of repeated calls"}
+    step_bytes = pattern.count("F") * idx_bytes + len(pattern) * attn_bytes
+    step_ms = (graph or {}).get("ms_per_token_step") or ms / steps_tok
     return {"value": cfg.B * steps_tok / (ms * 1e-3), "unit": "tok/s", "ms_per_token_step": ms / steps_tok,
             "steps": steps_tok, "batch": cfg.B, "context": cfg.q_pos0, "pattern": pattern,
-            "indexer_ms_per_F_layer": idx_layer_ms, "attn_ms_per_layer": attn_layer_ms,
+            "appends": "timed: one ic_decode_append launch per step (new token's k_I/scale on F layers, K/V on all)",
+            "indexer_ms_per_F_layer": idx_layer_ms, "attn_ms_per_layer": attn_layer_ms, "append_ms_per_step": append_ms,
+            "step_hbm_bytes": step_bytes,
+            "step_hbm_frac": step_bytes / (step_ms * 1e-3) / 1e9 / hbm,
             "kernels": roof, "clocks": clocks, "graph_replay": graph}
+
+
+def run_long(binding, pattern, seed, dev, gpu_index, peaks, n_chunks=None):
+    """The long-prefill workload: 47 layers, L = 204800 tokens prefilled in
+    chunks of 8192 query rows, each chunk over its whole causal prefix
+    (q_pos0 = 8192 c, S = 8192 (c + 1)), e4m3 indexer keys.  The key caches
+    (k_I + scale on the Full layers, K/V on all) are resident for the whole
+    run; each chunk's query-side inputs (q_I, w, Q) are drawn before its timed
+    forward.  Time = the sum over chunks of the ic_forward_pattern times."""
+    cfg = synth.LONG.with_(pattern=pattern)
+    L, C = cfg.S, cfg.chunk
+    n_chunks = L // C if n_chunks is None else n_chunks
+    n = cfg.n_layers
+    torch.cuda.synchronize()
+    caches = []
+    for l in range(n):
+        d = {}
+        if pattern[l] == "F":
+            _, d["kI"], d["kscale"], _ = synth.make_indexer_inputs(cfg, l, seed, dev, T=1, S=L)
+        _, d["K"], d["V"] = synth.make_attn_inputs(cfg, l, seed, dev, T=1, S=L)
+        caches.append(d)
+    O = [torch.empty((1, C, cfg.Hq, cfg.Dh), dtype=torch.bfloat16, device=dev) for _ in range(n)]
+    cache = torch.empty((1, C, cfg.k), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def chunk_layers(c):
+        layers = []
+        for l in range(n):
+            d = dict(caches[l])
+            if pattern[l] == "F":
+                d["q"], _, _, d["w"] = synth.make_indexer_inputs(cfg, l, seed, dev, T=C, S=1, t0=c * C)
+            d["Q"], _, _ = synth.make_attn_inputs(cfg, l, seed, dev, T=C, S=1, t0=c * C)
+            d["O"] = O[l]
+            layers.append(d)
+        return layers
+
+    # warm-up: the first and the last chunk once, untimed
+    for c in (0, n_chunks - 1):
+        f = binding.Forward(pattern, chunk_layers(c), cfg.k, c * C, (c + 1) * C, index_cache=cache)
+        f(stream)
+    torch.cuda.synchronize()
+    total_ms = 0.0
+    idx_ms = [0.0] * n
+    attn_ms = [0.0] * n
+    with ClockSampler(gpu_index) as clk:
+        for c in range(n_chunks):
+            layers = chunk_layers(c)
+            f = binding.Forward(pattern, layers, cfg.k, c * C, (c + 1) * C, index_cache=cache)
+            tr = binding.Trace(n, 1)
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            f(stream, trace=tr)
+            b.record(stream)
+            torch.cuda.synchronize()
+            total_ms += a.elapsed_time(b)
+            _, im, am = tr.read()
+            tr.close()
+            idx_ms = [x + y for x, y in zip(idx_ms, im)]
+            attn_ms = [x + y for x, y in zip(attn_ms, am)]
+            del layers, f
+    binding.stream_status()
+    clocks = clk.summary()
+    del caches, O, cache
+    torch.cuda.empty_cache()
+    Lp = n_chunks * C
+    n_f = pattern.count("F")
+    peak_tf = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    fl_i = 2.0 * cfg.H * cfg.D * (Lp * (Lp + 1) // 2)       # per F layer, all chunks
+    fl_a = sum(attn_flops(C, c * C, cfg.Hq, cfg.Dh, cfg.k) for c in range(n_chunks))
+    kern = {}
+    if n_f:
+        t = sum(idx_ms) / n_f
+        kern["indexer_topk"] = {"bound": "tensor", "achieved": fl_i / (t * 1e-3) / 1e12, "peak": peak_tf,
+                                "unit": "TFLOP/s", "frac": fl_i / (t * 1e-3) / 1e12 / peak_tf,
+                                "ms_per_F_layer_all_chunks": t, "flops_per_F_layer": fl_i}
+    t = sum(attn_ms) / n
+    kern["sparse_attn"] = {"bound": "tensor", "achieved": fl_a / (t * 1e-3) / 1e12, "peak": peak_tf,
+                           "unit": "TFLOP/s", "frac": fl_a / (t * 1e-3) / 1e12 / peak_tf,
+                           "ms_per_layer_all_chunks": t, "flops_per_layer": fl_a,
+                           "gathered_TB_per_s": fl_a / (4 * cfg.Hq * cfg.Dh) * 512 / (t * 1e-3) / 1e12}
+    return {"pattern": pattern, "tokens": Lp, "chunks": n_chunks, "chunk": C, "k_dtype": cfg.k_dtype,
+            "ms": total_ms, "value": Lp / (total_ms * 1e-3), "unit": "tok/s", "kernels": kern, "clocks": clocks}
 
 
 # ---------------------------------------------------------------------------
@@ -507,6 +672,8 @@ def ours_arm(args, world, rank, local):
         allf_res = {"pattern": "all-F (47 F)", "ms_per_step": ms_f,
                     "value": world * cfg.B * cfg.T / (ms_f * 1e-3), "unit": "tok/s", "steps": k_f,
                     "kernels": kernel_roofline(per_f, allf, cfg, peaks, k_f), "clocks": clk_f}
+        if not args.no_overlap:
+            allf_res["overlap_adjacent"] = adjacent_overlap(binding, layers, cfg)
 
     e2e = None
     if not args.no_e2e:
@@ -544,6 +711,16 @@ def ours_arm(args, world, rank, local):
         if df:
             decode["speedup_quarter_vs_allf"] = dq["value"] / df["value"]
 
+    long_res = None
+    if not args.no_long:
+        lq = run_long(binding, synth.LONG.pattern, seed + 5, dev, gpu_index, peaks)
+        lf = run_long(binding, "F" * 47, seed + 6, dev, gpu_index, peaks) if not args.no_allf else None
+        long_res = {"workload": "long: 47 layers, L=204800 prefilled in 25 chunks of 8192 query rows over the "
+                                "causal prefix, e4m3 indexer keys, H_I=64, d_I=128, k=2048; 32 q heads / 1 KV head, "
+                                "dim 128", "quarter_f": lq, "all_f": lf}
+        if lf:
+            long_res["speedup_quarter_vs_allf"] = lq["value"] / lf["value"]
+
     dom_name = max(kern, key=lambda n: kern[n]["total_ms_per_step"])
     dom = kern[dom_name]
     traffic = None
@@ -574,7 +751,7 @@ def ours_arm(args, world, rank, local):
             "gpu_launches": args.steps * launches_per_forward(quarter, cfg.B, cfg.T, cfg.k),
             "clocks": clocks, "all_f": allf_res, "e4m3_keys": e4,
             "speedup_quarter_vs_allf": (value / allf_res["value"]) if allf_res else None,
-            "decode": decode, "peaks": {k: v for k, v in peaks.items() if not k.startswith("_") and
+            "decode": decode, "long": long_res, "peaks": {k: v for k, v in peaks.items() if not k.startswith("_") and
                                         isinstance(v, (int, float))}}
     print(json.dumps(line), flush=True)
 
@@ -590,6 +767,8 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e4m3", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-long", action="store_true")
+    ap.add_argument("--no-overlap", action="store_true")
     ap.add_argument("--decode-steps", type=int, default=64)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--config", default="prefill32k", choices=["prefill32k", "short"],

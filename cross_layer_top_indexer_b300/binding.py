@@ -22,7 +22,7 @@ IC_BF16, IC_E4M3 = 0, 1
 EXPORTED = ("ic_workspace_size", "ic_indexer_topk", "ic_sparse_attn", "ic_forward_pattern",
             "ic_forward_pattern_traced", "ic_trace_create", "ic_trace_destroy", "ic_trace_read",
             "ic_stream_status", "ic_last_error", "ic_abi_version", "ic_indexer_topk_noalloc",
-            "ic_overlap", "ic_greedy_full_layers", "ic_debug_set_wait_limit_ns")
+            "ic_overlap", "ic_greedy_full_layers", "ic_debug_set_wait_limit_ns", "ic_decode_append")
 
 
 class IndexCacheError(RuntimeError):
@@ -51,6 +51,10 @@ class ICLayer(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("kI", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
                 ("w", ctypes.c_void_p), ("Q", ctypes.c_void_p), ("K", ctypes.c_void_p),
                 ("V", ctypes.c_void_p), ("O", ctypes.c_void_p)]
+
+
+class ICAppendSrc(ctypes.Structure):
+    _fields_ = [("kI", ctypes.c_void_p), ("k_scale", ctypes.c_void_p), ("K", ctypes.c_void_p), ("V", ctypes.c_void_p)]
 
 
 # double (*)(const char* pattern, void* user)
@@ -95,6 +99,9 @@ def load(path: str = LIB_PATH):
     lib.ic_abi_version.restype = i
     lib.ic_debug_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     lib.ic_debug_set_wait_limit_ns.restype = i
+    lib.ic_decode_append.argtypes = [ctypes.c_char_p, i, ctypes.POINTER(ICLayer), ctypes.POINTER(ICAppendSrc),
+                                     ctypes.POINTER(ICDims), i, vp]
+    lib.ic_decode_append.restype = i
     lib.ic_overlap.argtypes = [i, i, vp, vp, vp, vp, vp]
     lib.ic_overlap.restype = i
     lib.ic_greedy_full_layers.argtypes = [i, i, LOSS_FN, vp, ctypes.c_char_p, ctypes.POINTER(ctypes.c_longlong)]
@@ -363,6 +370,34 @@ def greedy_full_layers(n_layers: int, removals: int, evaluate_loss) -> tuple:
         raise failure[0]
     _raise(code)
     return out.value.decode(), fw.value
+
+
+class DecodeAppend:
+    """ic_decode_append prepared once: ``caches`` are the stack's layer dicts
+    (kI, kscale, K, V, ...), ``new_rows`` per-layer dicts of the new token's
+    rows (kI [B,D], kscale [B], K [B,Dh], V [B,Dh]).  Each call appends them
+    at row ``pos`` of every sequence, in one launch."""
+
+    def __init__(self, pattern: str, caches: Sequence[dict], new_rows: Sequence[dict], k_dtype: int):
+        load()
+        n = len(caches)
+        self.pattern = pattern.encode() if isinstance(pattern, str) else pattern
+        self.n = n
+        self.arr = (ICLayer * n)()
+        self.src = (ICAppendSrc * n)()
+        for l, (L, R) in enumerate(zip(caches, new_rows)):
+            self.arr[l] = ICLayer(_ptr(L.get("q")), _ptr(L.get("kI")), _ptr(L.get("kscale")), _ptr(L.get("w")),
+                                  _ptr(L["Q"]), _ptr(L["K"]), _ptr(L["V"]), _ptr(L.get("O")))
+            self.src[l] = ICAppendSrc(_ptr(R.get("kI")), _ptr(R.get("kscale")), _ptr(R["K"]), _ptr(R["V"]))
+        K0 = caches[0]["K"]
+        f0 = next((L for L, c in zip(caches, pattern) if c == "F"), caches[0])
+        D = f0["kI"].shape[-1] if f0.get("kI") is not None else 32
+        self.dims = make_dims(K0.shape[0], 1, K0.shape[1], 1, D, 1, 1, K0.shape[-1], 0, k_dtype, K0.shape[1])
+        self._keep = (caches, new_rows)
+
+    def __call__(self, pos: int, stream=None) -> None:
+        _raise(load().ic_decode_append(self.pattern, self.n, self.arr, self.src, ctypes.byref(self.dims), int(pos),
+                                       _stream(stream)))
 
 
 def stream_status(stream=None) -> None:

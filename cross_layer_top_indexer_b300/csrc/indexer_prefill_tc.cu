@@ -67,11 +67,19 @@ constexpr int CAP = kMaxK + 768;         // candidate slots per row
 constexpr int WG_THREADS = 128;
 constexpr int SEG = CAP / WG_THREADS;    // entries per thread in a cut
 constexpr int CUT_LIMIT = CAP - 2 * KT;  // a cut leaves room for at least two tiles
-constexpr int NWARPS = 10;               // bf16 keys
-constexpr int NTHREADS = NWARPS * 32;
-constexpr int CONV_THREADS = 64;         // e4m3 keys: two more warps
-constexpr int NTHREADS_E4M3 = NTHREADS + CONV_THREADS;
-constexpr int EPI_THREADS = 8 * 32;
+constexpr int CONV_THREADS = 64;         // e4m3 keys: two converter warps
+
+// Epilogue layout: bf16 keys run four warpgroups of one row each (four
+// epilogue warps per SM sub-partition hide the tensor-memory and barrier
+// latencies); e4m3 keys, whose converter warps need the registers, run two
+// warpgroups of two rows each.
+template <bool E4M3> struct Layout {
+  static constexpr int RPW = E4M3 ? 2 : 1;                   // rows per epilogue warpgroup
+  static constexpr int NWG = QPB / RPW;                      // epilogue warpgroups
+  static constexpr int EPI_THREADS = NWG * WG_THREADS;
+  static constexpr int CONV_WARP0 = 2 + NWG * 4;             // first converter warp (e4m3)
+  static constexpr int NTHREADS = EPI_THREADS + 64 + (E4M3 ? CONV_THREADS : 0);
+};
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = tc::idesc_bf16_f32(KT, NCOL);
 constexpr uint32_t IDESC_F16 = tc::idesc_f16_f32(KT, NCOL);
@@ -95,7 +103,7 @@ struct __align__(1024) TcSmem {
   int xc[2][QPB][4];
   uint32_t xmax[2][QPB][4];
   uint32_t xmin[2][QPB][4];
-  SelectScratch scr[2];
+  SelectScratch scr[QPB];
 };
 
 struct WgSync {
@@ -133,7 +141,7 @@ __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
 }
 
 template <bool E4M3>
-__global__ void __launch_bounds__(E4M3 ? NTHREADS_E4M3 : NTHREADS, 1)
+__global__ void __launch_bounds__(Layout<E4M3>::NTHREADS, 1)
 indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           IndexerArgs a, int n_groups, int* status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -153,7 +161,9 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
   const int n_keys = pos0 + nq;
   int32_t* out = a.idx + (static_cast<size_t>(b) * a.T + t0) * a.k;
 
-  constexpr int kThreads = E4M3 ? NTHREADS_E4M3 : NTHREADS;
+  using LY = Layout<E4M3>;
+  constexpr int kThreads = LY::NTHREADS;
+  constexpr int RPW = LY::RPW;
   if (n_keys <= a.k) {   // every causal position of every row is selected
     for (int i = tid; i < nq * a.k; i += kThreads) {
       const int qi = i / a.k, j = i - qi * a.k;
@@ -169,9 +179,9 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
       tc::mbar_init(&sm.full[s], E4M3 ? CONV_THREADS : 1);
       tc::mbar_init(&sm.empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) { tc::mbar_init(&sm.tfull[s], 1); tc::mbar_init(&sm.tempty[s], EPI_THREADS); }
+    for (int s = 0; s < 2; ++s) { tc::mbar_init(&sm.tfull[s], 1); tc::mbar_init(&sm.tempty[s], LY::EPI_THREADS); }
     tc::mbar_init(&sm.qfull, 1);
-    tc::mbar_init(&sm.qconv, EPI_THREADS);
+    tc::mbar_init(&sm.qconv, LY::EPI_THREADS);
     tc::mbar_init(&sm.drain, 1);
     sm.abort = 0;
     tc::fence_mbar_init();
@@ -195,9 +205,11 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
       tc::tma_prefetch_map(&tm_q);
       tc::tma_prefetch_map(&tm_k);
       const int qrow = (b * a.T + t0) * HH;
+      // q rows are read by this CTA only; key tiles by every CTA of the sequence
+      const uint64_t once = tc::l2_evict_first(), keep = tc::l2_evict_last();
       tc::mbar_arrive_expect_tx(&sm.qfull, 2 * NCOL * 128);
-      tc::tma_load_2d(sm.qb[0], &tm_q, &sm.qfull, 0, qrow);
-      tc::tma_load_2d(sm.qb[1], &tm_q, &sm.qfull, 64, qrow);
+      tc::tma_load_2d_hint(sm.qb[0], &tm_q, &sm.qfull, 0, qrow, once);
+      tc::tma_load_2d_hint(sm.qb[1], &tm_q, &sm.qfull, 64, qrow, once);
       const int krow0 = b * a.S_cap;
       int issued = 0;
       for (int it = 0; !E4M3 && it < 2 * nt; ++it) {
@@ -205,7 +217,7 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
         const uint32_t ph = (it / KSTAGES) & 1;
         if (!tc::mbar_wait(&sm.empty[s], ph ^ 1, &sm.abort, lim)) { set_abort(sm, status); break; }
         tc::mbar_arrive_expect_tx(&sm.full[s], KT * 128);
-        tc::tma_load_2d(sm.kst[s], &tm_k, &sm.full[s], (it & 1) * 64, krow0 + (it >> 1) * KT);
+        tc::tma_load_2d_hint(sm.kst[s], &tm_k, &sm.full[s], (it & 1) * 64, krow0 + (it >> 1) * KT, keep);
         issued = it + 1;
       }
       // no copy of ours may still be landing in shared memory when the CTA exits
@@ -247,10 +259,10 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
       if (!tc::mbar_wait(&sm.drain, 0, nullptr, 4000000000ull)) set_abort(sm, status);
     }
     __syncwarp();
-  } else if (warp >= NWARPS) {
+  } else if (warp >= LY::CONV_WARP0) {
     // ================= e4m3 keys -> f16 operand tiles =================
     if constexpr (E4M3) {
-      const int ct = tid - NTHREADS;                // 0..63
+      const int ct = tid - LY::CONV_WARP0 * 32;     // 0..63
       const uint8_t* kbase = static_cast<const uint8_t*>(a.kI);
       const long long krow0 = static_cast<long long>(b) * a.S_cap;
       const long long nrows = static_cast<long long>(a.B) * a.S_cap;
@@ -305,19 +317,20 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
     }
   } else {
     // ================= epilogue: scores + streaming top-k =================
-    const int wg = (warp - 2) >> 2;               // warpgroup 0 / 1
+    const int wg = (warp - 2) >> 2;               // epilogue warpgroup
     const int quarter = warp & 3;                 // TMEM lane quarter this warp may read
     const int key_local = quarter * 32 + lane;
     const int wtid = tid - 64 - wg * WG_THREADS;  // 0..127 within the warpgroup
     const WgSync wsync{1 + wg};
     const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
-    const int q0 = 2 * wg;
+    const int q0 = RPW * wg;                      // this warpgroup's rows q0 .. q0 + RPW - 1
     const unsigned lanes_below = (1u << lane) - 1u;
     // per-row state, identical in every thread of the warpgroup
-    int cnt[2] = {0, 0};
-    uint32_t tau[2] = {0u, 0u};                     // a key enters iff key > tau
-    uint32_t rmin[2] = {0xFFFFFFFFu, 0xFFFFFFFFu};  // bounds of the keys in the list
-    uint32_t rmax[2] = {0u, 0u};
+    int cnt[RPW];
+    uint32_t tau[RPW];                              // a key enters iff key > tau
+    uint32_t rmin[RPW], rmax[RPW];                  // bounds of the keys in the list
+#pragma unroll
+    for (int qq = 0; qq < RPW; ++qq) { cnt[qq] = 0; tau[qq] = 0u; rmin[qq] = 0xFFFFFFFFu; rmax[qq] = 0u; }
 
     if constexpr (E4M3) {
       // this warpgroup's two q rows: thread = (row q0 + wtid / 64, head wtid % 64)
@@ -375,31 +388,39 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
       const bool ok = tc::mbar_wait(&sm.tfull[acc], (j >> 1) & 1, &sm.abort, lim);
       if (!ok) set_abort(sm, status);
       tc::tc_fence_after();
-      uint32_t key[2];
+      uint32_t key[RPW];
 #pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {
+      for (int qq = 0; qq < RPW; ++qq) {
         const uint32_t col = tmem + lane_field + acc * NCOL + (q0 + qq) * HH;
-        uint32_t r0[32], r1[32];
-        tc::tmem_ld_x32(col, r0);
-        tc::tmem_ld_x32(col + 32, r1);
-        tc::tmem_wait_ld();
         const float* wq = sm.wsm[q0 + qq];
         float s0 = 0.0f, s1 = 0.0f, s2 = 0.0f, s3 = 0.0f;   // four chains: the FMA latencies overlap
+        auto accumulate = [&](const uint32_t (&r)[32], const float* wh) {
 #pragma unroll
-        for (int h = 0; h < 32; h += 4) {
-          const float4 w4 = *reinterpret_cast<const float4*>(wq + h);
-          s0 = fmaf(w4.x, fmaxf(__uint_as_float(r0[h + 0]), 0.0f), s0);
-          s1 = fmaf(w4.y, fmaxf(__uint_as_float(r0[h + 1]), 0.0f), s1);
-          s2 = fmaf(w4.z, fmaxf(__uint_as_float(r0[h + 2]), 0.0f), s2);
-          s3 = fmaf(w4.w, fmaxf(__uint_as_float(r0[h + 3]), 0.0f), s3);
-        }
-#pragma unroll
-        for (int h = 0; h < 32; h += 4) {
-          const float4 w4 = *reinterpret_cast<const float4*>(wq + 32 + h);
-          s0 = fmaf(w4.x, fmaxf(__uint_as_float(r1[h + 0]), 0.0f), s0);
-          s1 = fmaf(w4.y, fmaxf(__uint_as_float(r1[h + 1]), 0.0f), s1);
-          s2 = fmaf(w4.z, fmaxf(__uint_as_float(r1[h + 2]), 0.0f), s2);
-          s3 = fmaf(w4.w, fmaxf(__uint_as_float(r1[h + 3]), 0.0f), s3);
+          for (int h = 0; h < 32; h += 4) {
+            const float4 w4 = *reinterpret_cast<const float4*>(wh + h);
+            s0 = fmaf(w4.x, fmaxf(__uint_as_float(r[h + 0]), 0.0f), s0);
+            s1 = fmaf(w4.y, fmaxf(__uint_as_float(r[h + 1]), 0.0f), s1);
+            s2 = fmaf(w4.z, fmaxf(__uint_as_float(r[h + 2]), 0.0f), s2);
+            s3 = fmaf(w4.w, fmaxf(__uint_as_float(r[h + 3]), 0.0f), s3);
+          }
+        };
+        if constexpr (RPW == 1) {
+          // one half of the heads at a time (fewer live registers; the other
+          // epilogue warps of the sub-partition cover the load latency)
+          uint32_t r[32];
+          tc::tmem_ld_x32(col, r);
+          tc::tmem_wait_ld();
+          accumulate(r, wq);
+          tc::tmem_ld_x32(col + 32, r);
+          tc::tmem_wait_ld();
+          accumulate(r, wq + 32);
+        } else {
+          uint32_t r0[32], r1[32];
+          tc::tmem_ld_x32(col, r0);
+          tc::tmem_ld_x32(col + 32, r1);
+          tc::tmem_wait_ld();
+          accumulate(r0, wq);
+          accumulate(r1, wq + 32);
         }
         key[qq] = float_key(E4M3 ? ((s0 + s1) + (s2 + s3)) * ks : (s0 + s1) + (s2 + s3));
       }
@@ -408,10 +429,10 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
 
       // this warp's candidates of the tile; counts and key bounds go to the other warps
       const int s_pos = j * KT + key_local;
-      bool valid[2], take[2];
-      unsigned bal[2];
+      bool valid[RPW], take[RPW];
+      unsigned bal[RPW];
 #pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {
+      for (int qq = 0; qq < RPW; ++qq) {
         const int qi = q0 + qq;
         valid[qq] = qi < nq && s_pos <= pos0 + qi;
         take[qq] = valid[qq] && key[qq] > tau[qq];
@@ -427,7 +448,7 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
       // the tile's one barrier: the exchange, and one abort decision for the warpgroup
       if (tc::named_sync_or(1 + wg, WG_THREADS, !ok || sm.abort)) { aborted = true; break; }
 #pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {
+      for (int qq = 0; qq < RPW; ++qq) {
         const int qi = q0 + qq;
         int tot = sm.xc[par][qi][0] + sm.xc[par][qi][1] + sm.xc[par][qi][2] + sm.xc[par][qi][3];
         if (cnt[qq] + tot > CAP) {
@@ -462,7 +483,7 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
     // exact cut to k and write-out (ascending already)
     if (!aborted) {
 #pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {
+      for (int qq = 0; qq < RPW; ++qq) {
         const int qi = q0 + qq;
         if (qi >= nq) break;
         int c = cnt[qq];
@@ -506,7 +527,8 @@ cudaError_t launch_indexer_prefill_tc(const IndexerArgs& a, int* dev_status, cud
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(n_groups, a.B);
-  kern<<<grid, a.e4m3 ? NTHREADS_E4M3 : NTHREADS, smem, st>>>(tm_q, tm_k, a, n_groups, dev_status);
+  kern<<<grid, a.e4m3 ? Layout<true>::NTHREADS : Layout<false>::NTHREADS, smem, st>>>(tm_q, tm_k, a, n_groups,
+                                                                                   dev_status);
   return cudaGetLastError();
 }
 

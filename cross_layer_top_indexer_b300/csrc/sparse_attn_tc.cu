@@ -239,30 +239,40 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     const uint32_t n_items = 2u * n_tiles;
     const uint64_t keep = tc::l2_evict_last();       // K/V rows are re-read by many rows
     uint4 buf[2][PROD_ROWS];
+    int sidx[PROD_ROWS];                             // source rows of the current tile (-1: empty slot)
+    size_t base_row = 0;
     bool ok = true;
-    // issue the loads of item it into buf[it & 1]; returns false on abort
+    // loads of item it into registers; K items (even) first fetch the tile's
+    // index entries, which the tile's V item reuses.  No ring slot is held
+    // while the loads are in flight.
     auto issue = [&](uint32_t it, uint4 (&b)[PROD_ROWS]) -> bool {
-      const uint32_t tile = it >> 1;
-      const int n = static_cast<int>(tile / nt);
-      const int j = static_cast<int>(tile % nt);
-      const int qb = n & 1;
-      if (j == 0 && (it & 1) == 0 && !tc::mbar_wait(&sm.qfull[qb], (n >> 1) & 1, &sm.abort)) return false;
-      if (!tc::mbar_wait(&sm.empty[it % NSLOT], ((it / NSLOT) & 1) ^ 1, &sm.abort)) return false;
-      const int row = static_cast<int>(blockIdx.x) + n * static_cast<int>(gridDim.x);
-      const size_t base_row = static_cast<size_t>(row / a.T) * a.S_cap;
-      const uint4* g = ((it & 1) ? Vg : Kg) + base_row * (DH / 8);
-      const int32_t* irow = sm.idx[qb] + j * KT;
-      const int lim = k - j * KT;                    // positions past k are empty slots
+      if ((it & 1) == 0) {
+        const uint32_t tile = it >> 1;
+        const int n = static_cast<int>(tile / nt);
+        const int j = static_cast<int>(tile % nt);
+        const int qb = n & 1;
+        if (j == 0 && !tc::mbar_wait(&sm.qfull[qb], (n >> 1) & 1, &sm.abort)) return false;
+        const int row = static_cast<int>(blockIdx.x) + n * static_cast<int>(gridDim.x);
+        base_row = static_cast<size_t>(row / a.T) * a.S_cap;
+        const int32_t* irow = sm.idx[qb] + j * KT;
+        const int lim = k - j * KT;                  // positions past k are empty slots
 #pragma unroll
-      for (int i = 0; i < PROD_ROWS; ++i) {
-        const int r = r0 + RSTEP * i;
-        const int s = r < lim ? irow[r] : -1;
-        b[i] = (s >= 0 && s < a.S) ? tc::ldg16_hint(g + static_cast<size_t>(s) * (DH / 8), keep)
-                                   : make_uint4(0u, 0u, 0u, 0u);
+        for (int i = 0; i < PROD_ROWS; ++i) {
+          const int r = r0 + RSTEP * i;
+          const int s = r < lim ? irow[r] : -1;
+          sidx[i] = (s >= 0 && s < a.S) ? s : -1;
+        }
       }
+      const uint4* g = ((it & 1) ? Vg : Kg) + base_row * (DH / 8);
+#pragma unroll
+      for (int i = 0; i < PROD_ROWS; ++i)
+        b[i] = sidx[i] >= 0 ? tc::ldg16_hint(g + static_cast<size_t>(sidx[i]) * (DH / 8), keep)
+                            : make_uint4(0u, 0u, 0u, 0u);
       return true;
     };
-    auto store = [&](uint32_t it, const uint4 (&b)[PROD_ROWS]) {
+    // the ring slot is taken only when the data is about to be written
+    auto store = [&](uint32_t it, const uint4 (&b)[PROD_ROWS]) -> bool {
+      if (!tc::mbar_wait(&sm.empty[it % NSLOT], ((it / NSLOT) & 1) ^ 1, &sm.abort)) return false;
       uint8_t* dst = sm.ring[it % NSLOT] + half * HALF_BYTES;
 #pragma unroll
       for (int i = 0; i < PROD_ROWS; ++i) {
@@ -271,14 +281,15 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       }
       tc::fence_proxy_async_smem();
       tc::mbar_arrive(&sm.full[it % NSLOT]);
+      return true;
     };
     if (n_items > 0) ok = issue(0, buf[0]);
     for (uint32_t it = 0; ok && it < n_items; it += 2) {
       // item it (K) is in buf[0]; item it + 1 (V of the same tile) always exists
       if (!(ok = issue(it + 1, buf[1]))) break;
-      store(it, buf[0]);
+      if (!(ok = store(it, buf[0]))) break;
       if (it + 2 < n_items && !(ok = issue(it + 2, buf[0]))) break;
-      store(it + 1, buf[1]);
+      if (!(ok = store(it + 1, buf[1]))) break;
     }
     if (!ok) set_abort(sm, status);
   } else if (warp == MMA_WARP) {

@@ -163,6 +163,31 @@ ic_status ic_forward_pattern(const char* pattern, int n_layers, const ic_layer* 
                              const ic_dims* dims, int32_t* index_cache, int* indexer_calls,
                              void* ws, size_t ws_bytes, void* stream);
 
+/* Rows of one new token per sequence, for ic_decode_append (device
+ * pointers; kI and k_scale are read on Full layers only). */
+typedef struct ic_append_src {
+  const void* kI;        /* [B, D] bf16, or e4m3 bytes                             */
+  const float* k_scale;  /* [B] fp32 > 0 (IC_E4M3 only)                            */
+  const void* K;         /* [B, Dh] bf16                                           */
+  const void* V;         /* [B, Dh] bf16                                           */
+} ic_append_src;
+
+/* Decode step, append (notes page, "背景 & 问题提出": each query's indexer
+ * scores all tokens before it; a decoded token's own keys join the caches
+ * before its query runs): for every layer l and sequence b, copies
+ * src[l].K[b], src[l].V[b] into layers[l].K / .V at row pos of sequence b, and
+ * on Full layers src[l].kI[b] (and k_scale[b]) into layers[l].kI (.k_scale).
+ * One launch for the whole stack.  `layers` and `src` are HOST arrays of
+ * n_layers entries (at most 64); the pattern is checked as in
+ * ic_forward_pattern.  Uses dims->B, S_cap (0 means S), D, Dh and k_dtype;
+ * 0 <= pos < S_cap.  A decode step is this call, then ic_forward_pattern
+ * with q_pos0 = pos, T = 1 and S = pos + 1.
+ * Errors: IC_ERR_PATTERN, IC_ERR_ARG (null or misaligned pointers, pos out of
+ * range), IC_ERR_UNSUPPORTED (more than 64 layers, D or Dh unsupported),
+ * IC_ERR_CUDA. */
+ic_status ic_decode_append(const char* pattern, int n_layers, const ic_layer* layers, const ic_append_src* src,
+                           const ic_dims* dims, int pos, void* stream);
+
 /* Per-layer tracing of the F/S loop.  The deep-read page's measurement
  * section ("一个实用的测量顺序") asks for the indexer time and the core
  * sparse-attention time of every layer before any end-to-end figure.  A

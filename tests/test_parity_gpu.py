@@ -503,12 +503,15 @@ def test_decode_full_size_sampled():
 
 
 @pytest.mark.slow
-def test_long_last_chunk_sampled():
-    # the last 8192-query chunk of the 204800-token prefill, fp8 keys
+@pytest.mark.parametrize("chunk", [0, 12, 24])
+def test_long_chunk_sampled(chunk):
+    # the first, a middle and the last 8192-query chunk of the 204800-token
+    # prefill (queries over the whole causal prefix), fp8 keys
     cfg = synth.LONG.with_(n_layers=2, pattern="FS", T=8192)
-    q_pos0 = 204800 - 8192
-    layers = synth.make_stack(cfg, 555, DEV, T=8192, S=204800)
-    _stack_check(cfg, layers, _sample_rows(8192, 0, 6, 3), 555, q_pos0=q_pos0, S=204800)
+    q_pos0 = chunk * 8192
+    layers = synth.make_stack(cfg, 555 + chunk, DEV, T=8192, S=204800)
+    rows = _sample_rows(8192, 2048 if chunk == 0 else 0, 6, 3 + chunk)
+    _stack_check(cfg, layers, rows, 555 + chunk, q_pos0=q_pos0, S=204800)
 
 
 def test_bad_pattern_launches_nothing():
