@@ -22,7 +22,8 @@ IC_BF16, IC_E4M3 = 0, 1
 EXPORTED = ("ic_workspace_size", "ic_indexer_topk", "ic_sparse_attn", "ic_forward_pattern",
             "ic_forward_pattern_traced", "ic_trace_create", "ic_trace_destroy", "ic_trace_read",
             "ic_stream_status", "ic_last_error", "ic_abi_version", "ic_indexer_topk_noalloc",
-            "ic_overlap", "ic_greedy_full_layers", "ic_debug_set_wait_limit_ns", "ic_decode_append")
+            "ic_overlap", "ic_greedy_full_layers", "ic_debug_set_wait_limit_ns", "ic_decode_append",
+            "ic_indexer_topk_fp8")
 
 
 class IndexCacheError(RuntimeError):
@@ -77,6 +78,8 @@ def load(path: str = LIB_PATH):
     lib.ic_indexer_topk.argtypes = [i, i, i, i, i, i, i, i, vp, vp, i, vp, vp, vp, vp, sz, vp]
     lib.ic_indexer_topk.restype = i
     lib.ic_indexer_topk_noalloc.argtypes = [i, i, i, i, i, i, i, i, vp, vp, i, vp, vp, vp, vp]
+    lib.ic_indexer_topk_fp8.argtypes = [i, i, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp]
+    lib.ic_indexer_topk_fp8.restype = i
     lib.ic_indexer_topk_noalloc.restype = i
     lib.ic_sparse_attn.argtypes = [i, i, i, i, i, i, i, vp, vp, vp, vp, f, vp, vp, sz, vp]
     lib.ic_sparse_attn.restype = i
@@ -182,6 +185,22 @@ def indexer_topk(q: torch.Tensor, kI: torch.Tensor, w: torch.Tensor, k: int, q_p
     wsp, wsb = _workspace(workspace_size(dims), ws, q.device)
     code = lib.ic_indexer_topk(B, T, S, S_cap, H, D, k, q_pos0, _ptr(q), _ptr(kI), _kdtype(kI), _ptr(kscale),
                                _ptr(w), _ptr(idx_out), wsp, wsb, _stream(stream))
+    _raise(code)
+    return idx_out
+
+
+def indexer_topk_fp8(q8: torch.Tensor, q_scale: torch.Tensor, kI: torch.Tensor, kscale: torch.Tensor,
+                     w: torch.Tensor, k: int, q_pos0: int = 0, S: Optional[int] = None,
+                     idx_out: Optional[torch.Tensor] = None, stream=None):
+    """ic_indexer_topk_fp8: q8 [B,T,H,D] e4m3, q_scale [B,T,H], kI [B,S_cap,D] e4m3, kscale [B,S_cap]."""
+    lib = load()
+    B, T, H, D = q8.shape
+    S_cap = kI.shape[1]
+    S = q_pos0 + T if S is None else S
+    if idx_out is None:
+        idx_out = torch.empty((B, T, k), dtype=torch.int32, device=q8.device)
+    code = lib.ic_indexer_topk_fp8(B, T, S, S_cap, H, D, k, q_pos0, _ptr(q8), _ptr(q_scale), _ptr(kI), _ptr(kscale),
+                                   _ptr(w), _ptr(idx_out), _stream(stream))
     _raise(code)
     return idx_out
 

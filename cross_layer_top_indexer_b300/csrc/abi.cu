@@ -114,8 +114,9 @@ ic_status check_indexer_args(int B, int T, int S, int S_cap, int H, int D, int k
 
 namespace {
 
-size_t indexer_ws(int B, int T, int S) {
-  return T <= ic::kDecodeMaxT ? ic::indexer_decode_ws_fast_bytes(B, T, S) : 0;
+size_t indexer_ws(const ic_dims* d) {
+  if (d->T <= ic::kDecodeMaxT) return ic::indexer_decode_ws_fast_bytes(d->B, d->T, d->S);
+  return ic::indexer_prefill_tc_ws_bytes(d->B, d->T, d->S, d->H, d->D, d->k_dtype == IC_E4M3);
 }
 
 ic_status cuda_fail(cudaError_t e, const char* what) {
@@ -133,7 +134,11 @@ ic_status run_indexer(ic::IndexerArgs a, void* ws, size_t ws_bytes, cudaStream_t
     if (need && !aligned16(ws)) return fail(IC_ERR_ARG, "workspace must be 16-byte aligned");
     e = ic::launch_indexer_decode(a, ws, ws_bytes, status, st);
   } else if (ic::indexer_prefill_tc_supported(a)) {
-    e = ic::launch_indexer_prefill_tc(a, status, st);
+    const size_t need = ic::indexer_prefill_tc_ws_bytes(a.B, a.T, a.S, a.H, a.D, a.e4m3 != 0);
+    if (ws_bytes < need || (need && !ws))
+      return fail(IC_ERR_ARG, "workspace of %zu bytes is smaller than the %zu needed", ws_bytes, need);
+    if (need && !aligned16(ws)) return fail(IC_ERR_ARG, "workspace must be 16-byte aligned");
+    e = ic::launch_indexer_prefill_tc(a, ws, ws_bytes, status, st);
   } else {
     e = ic::launch_indexer_prefill(a, status, st);
   }
@@ -169,7 +174,7 @@ IC_EXPORT const char* ic_last_error(void) { return g_msg; }
 
 IC_EXPORT size_t ic_workspace_size(const ic_dims* d) {
   if (!d || d->B < 1 || d->T < 1 || d->S < 1 || d->k < 1 || d->Hq < 1 || d->Dh < 1) return (size_t)-1;
-  const size_t a = indexer_ws(d->B, d->T, d->S);
+  const size_t a = indexer_ws(d);
   const size_t b = ic::attn_ws_bytes(d->B, d->T, d->Hq, d->Dh, d->k);
   return a > b ? a : b;
 }
@@ -183,6 +188,25 @@ IC_EXPORT ic_status ic_indexer_topk(int B, int T, int S, int S_cap, int H, int D
   if (st != IC_OK) return st;
   ic::IndexerArgs a{q, kI, k_scale, w, idx_out, B, T, S, S_cap, H, D, k, q_pos0, k_dtype == IC_E4M3};
   return run_indexer(a, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+IC_EXPORT ic_status ic_indexer_topk_fp8(int B, int T, int S, int S_cap, int H, int D, int k, int q_pos0,
+                                        const void* q, const float* q_scale, const void* kI, const float* k_scale,
+                                        const float* w, int32_t* idx_out, void* stream) {
+  g_msg[0] = 0;
+  if (S_cap == 0) S_cap = S;
+  ic_status st = check_indexer(B, T, S, S_cap, H, D, k, q_pos0, q, kI, IC_E4M3, k_scale, w, idx_out);
+  if (st != IC_OK) return st;
+  if (!q_scale) return fail(IC_ERR_ARG, "e4m3 queries need q_scale");
+  if (!aligned16(q_scale)) return fail(IC_ERR_ARG, "tensor pointers must be 16-byte aligned");
+  if (H != 64 || D != 128 || T <= ic::kDecodeMaxT)
+    return fail(IC_ERR_UNSUPPORTED, "e4m3 queries: the kernel covers H=64, D=128 and more than %d query rows "
+                "(got H=%d D=%d T=%d)", ic::kDecodeMaxT, H, D, T);
+  ic::IndexerArgs a{q, kI, k_scale, w, idx_out, B, T, S, S_cap, H, D, k, q_pos0, 1};
+  a.qscale = q_scale;
+  a.wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+  cudaError_t e = ic::launch_indexer_prefill_tc(a, nullptr, 0, device_status_ptr(), static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? IC_OK : cuda_fail(e, "indexer launch");
 }
 
 IC_EXPORT ic_status ic_sparse_attn(int B, int T, int S, int S_cap, int Hq, int Dh, int k, const void* Q, const void* K,

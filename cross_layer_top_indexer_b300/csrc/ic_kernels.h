@@ -18,6 +18,7 @@ struct IndexerArgs {
   int32_t* idx;          // [B,T,k]
   int B, T, S, S_cap, H, D, k, q_pos0, e4m3;
   uint64_t wait_ns = 0;  // limit of the tensor-core prefill kernel's waits; 0 = kWaitLimitNs
+  const float* qscale = nullptr;   // [B,T,H] > 0: q given as e4m3 bytes (tensor-core prefill kernel only)
 };
 
 struct AttnArgs {
@@ -33,7 +34,10 @@ struct AttnArgs {
 // Fused prefill indexer + streaming top-k (scores never leave the SM).
 // Tensor-core (tcgen05/TMA) kernel for H = 64, D = 128, bf16 keys:
 bool indexer_prefill_tc_supported(const IndexerArgs& a);
-cudaError_t launch_indexer_prefill_tc(const IndexerArgs& a, int* dev_status, cudaStream_t st);
+// Workspace of the tensor-core prefill path (e4m3 keys: their bf16 widening).
+size_t indexer_prefill_tc_ws_bytes(int B, int T, int S, int H, int D, bool e4m3);
+cudaError_t launch_indexer_prefill_tc(const IndexerArgs& a, void* ws, size_t ws_bytes, int* dev_status,
+                                      cudaStream_t st);
 // mma.sync kernel for every other supported shape:
 cudaError_t launch_indexer_prefill(const IndexerArgs& a, int* dev_status, cudaStream_t st);
 

@@ -9,28 +9,23 @@
 // One CTA owns QPB = 4 consecutive query rows.  Their q rows form the MMA's
 // B operand (N = 4 x 64 = 256 columns, loaded once by TMA); key tiles of
 // 128 rows form the A operand (M = 128, keys on the TMEM lanes), streamed by
-// TMA in K-halves of 64 features through a 3-deep ring.  One thread issues
+// TMA in K-halves of 64 features through a 4-deep ring.  One thread issues
 // the MMAs into two TMEM accumulators of 128 x 256 fp32 (all 512 columns),
 // so the tensor core fills one while the epilogue drains the other.
 //
-// Warp roles (10 warps; 12 for e4m3 keys):
-//   warp 0     TMA producer (q once, then key half-tiles; for e4m3 keys only q)
+// Warp roles (18 warps):
+//   warp 0     TMA producer (q once, then key half-tiles)
 //   warp 1     TMEM allocator + MMA issuer
-//   warps 2-9  epilogue: two warpgroups; warpgroup g owns query rows 2g and
-//              2g+1.  Thread = one key (its TMEM lane); it reads the 64 head
-//              dot products of each of its two rows, forms the weighted ReLU
+//   warps 2-17 epilogue: four warpgroups; warpgroup g owns query row g.
+//              Thread = one key (its TMEM lane); it reads the 64 head dot
+//              products of its row in two halves, forms the weighted ReLU
 //              sum in registers, and runs the streaming top-k.
-//   warps 10-11 (e4m3 keys) widen each key tile from global memory into the
-//              ring as f16, exactly (every e4m3 value is an f16), with the
-//              hardware conversion.
 //
-// e4m3 keys: the MMA runs on f16 operands (kind::f16).  Each bf16 q row is
-// rewritten in place as f16 times a power of two 2^e_h that brings its
-// largest magnitude into [2^14, 2^15); f16 has 11 significant bits against
-// bf16's 8, so every element not below 2^-17 after scaling (a relative
-// 2^-31 of the row's largest) is carried exactly.  The weight w_h is
-// multiplied by 2^-e_h, so the epilogue is unchanged, and the key's scale
-// multiplies the score (a positive factor commutes with ReLU).
+// e4m3 keys: every e4m3 value (subnormals included) is a bf16 value, so a
+// small kernel first widens the keys the call reads into a bf16 copy in the
+// workspace, exactly; the same TMA-fed kernel then runs on bf16 q and keys,
+// and the key's scale multiplies its head sum (a positive factor commutes
+// with ReLU).  No operand is rounded.
 //
 // Streaming top-k (per row, in shared memory): a candidate list of (key,
 // position), key = an order-preserving integer image of the score, kept in
@@ -54,6 +49,8 @@
 #include "tc_utils.cuh"
 #include "topk_stream.cuh"
 
+#include <algorithm>
+
 namespace ic {
 namespace {
 
@@ -67,22 +64,26 @@ constexpr int CAP = kMaxK + 768;         // candidate slots per row
 constexpr int WG_THREADS = 128;
 constexpr int SEG = CAP / WG_THREADS;    // entries per thread in a cut
 constexpr int CUT_LIMIT = CAP - 2 * KT;  // a cut leaves room for at least two tiles
-constexpr int CONV_THREADS = 64;         // e4m3 keys: two converter warps
 
-// Epilogue layout: bf16 keys run four warpgroups of one row each (four
-// epilogue warps per SM sub-partition hide the tensor-memory and barrier
-// latencies); e4m3 keys, whose converter warps need the registers, run two
-// warpgroups of two rows each.
-template <bool E4M3> struct Layout {
-  static constexpr int RPW = E4M3 ? 2 : 1;                   // rows per epilogue warpgroup
+// Epilogue layout: four warpgroups of one row each (four epilogue warps per
+// SM sub-partition hide the tensor-memory and barrier latencies).
+struct Layout {
+  static constexpr int RPW = 1;                              // rows per epilogue warpgroup
   static constexpr int NWG = QPB / RPW;                      // epilogue warpgroups
   static constexpr int EPI_THREADS = NWG * WG_THREADS;
-  static constexpr int CONV_WARP0 = 2 + NWG * 4;             // first converter warp (e4m3)
-  static constexpr int NTHREADS = EPI_THREADS + 64 + (E4M3 ? CONV_THREADS : 0);
+  static constexpr int NTHREADS = EPI_THREADS + 64;
+};
+
+// Operand kinds of the kernel.
+enum Kind : int {
+  KEYS_BF16 = 0,   // bf16 q and keys (kind::f16)
+  KEYS_E4M3 = 1,   // bf16 q, e4m3 keys widened to bf16 in the workspace, per-key scale in the epilogue
+  QK_E4M3 = 2,     // e4m3 q and keys as stored (kind::f8f6f4), per-(row, head) q scale folded into w,
+                   // per-key scale in the epilogue
 };
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = tc::idesc_bf16_f32(KT, NCOL);
-constexpr uint32_t IDESC_F16 = tc::idesc_f16_f32(KT, NCOL);
+constexpr uint32_t IDESC_E4M3 = tc::idesc_e4m3_f32(KT, NCOL);
 
 struct __align__(1024) TcSmem {
   uint8_t qb[2][NCOL * 128];             // B operand: two K-halves, 256 rows x 128 B (SW128)
@@ -95,7 +96,6 @@ struct __align__(1024) TcSmem {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t qfull;
-  uint64_t qconv;                        // e4m3 keys: q rewritten as scaled f16
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -116,34 +116,38 @@ __device__ __forceinline__ void set_abort(TcSmem& sm, int* status) {
   if (status) atomicExch(status, kDevTimeout);
 }
 
-// Eight bf16 (one 16-byte chunk) -> eight floats.
-__device__ __forceinline__ void bf16x8_to_f32(const uint4& c, float* f) {
-  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    f[2 * j] = __uint_as_float(w[j] << 16);
-    f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+// e4m3 byte pairs -> bf16 pairs, exactly: every e4m3 value (subnormals
+// included) is a bf16 value.  Normal codes move the exponent from bias 7 to
+// bias 127 and the 3 mantissa bits to the top of bf16's 7; subnormal codes
+// (exponent field 0) are m * 2^-9.
+__device__ __forceinline__ uint32_t e4m3_pair_to_bf16_pair(uint32_t v) {
+  return e4m3_to_bf16_bits(v & 0xFFu) | (e4m3_to_bf16_bits((v >> 8) & 0xFFu) << 16);
+}
+
+// e4m3 keys [B, S_cap, 128] (rows 0 .. S-1 of each sequence) -> bf16 keys
+// [B, S, 128], one 16-byte chunk of 16 codes per thread.
+__global__ void __launch_bounds__(256) widen_e4m3_keys_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                              int B, int S, int S_cap) {
+  const size_t per_seq = static_cast<size_t>(S) * (DD / 16);
+  const size_t n_chunks = per_seq * B;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_chunks;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
+    const size_t b = i / per_seq, r = i - b * per_seq;
+    const uint4 x = __ldcs(src + b * static_cast<size_t>(S_cap) * (DD / 16) + r);
+    uint4 lo, hi;
+    lo.x = e4m3_pair_to_bf16_pair(x.x);       lo.y = e4m3_pair_to_bf16_pair(x.x >> 16);
+    lo.z = e4m3_pair_to_bf16_pair(x.y);       lo.w = e4m3_pair_to_bf16_pair(x.y >> 16);
+    hi.x = e4m3_pair_to_bf16_pair(x.z);       hi.y = e4m3_pair_to_bf16_pair(x.z >> 16);
+    hi.z = e4m3_pair_to_bf16_pair(x.w);       hi.w = e4m3_pair_to_bf16_pair(x.w >> 16);
+    dst[2 * i] = lo;
+    dst[2 * i + 1] = hi;
   }
 }
 
-// Two e4m3 bytes (the low 16 bits, low byte first) -> two f16, exactly.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
-  uint32_t h2;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(v)));
-  return h2;
-}
-
-// Two floats -> packed f16x2 (round to nearest), `lo` in the low half.
-__device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-template <bool E4M3>
-__global__ void __launch_bounds__(Layout<E4M3>::NTHREADS, 1)
+template <int KIND>
+__global__ void __launch_bounds__(Layout::NTHREADS, 1)
 indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                          IndexerArgs a, int n_groups, int* status) {
+                          IndexerArgs a, int n_groups, int key_rows, int* status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // the dynamic shared window is 1024-aligned for the swizzled operands
   TcSmem& sm = *reinterpret_cast<TcSmem*>(
@@ -161,7 +165,9 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
   const int n_keys = pos0 + nq;
   int32_t* out = a.idx + (static_cast<size_t>(b) * a.T + t0) * a.k;
 
-  using LY = Layout<E4M3>;
+  using LY = Layout;
+  constexpr bool E4M3 = KIND != KEYS_BF16;      // a per-key scale multiplies the head sum
+  constexpr bool FP8 = KIND == QK_E4M3;         // 8-bit operands: one 16 KB stage per 128-key tile
   constexpr int kThreads = LY::NTHREADS;
   constexpr int RPW = LY::RPW;
   if (n_keys <= a.k) {   // every causal position of every row is selected
@@ -176,19 +182,20 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
   // ---- set-up ----
   if (tid == 0) {
     for (int s = 0; s < KSTAGES; ++s) {
-      tc::mbar_init(&sm.full[s], E4M3 ? CONV_THREADS : 1);
+      tc::mbar_init(&sm.full[s], 1);
       tc::mbar_init(&sm.empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) { tc::mbar_init(&sm.tfull[s], 1); tc::mbar_init(&sm.tempty[s], LY::EPI_THREADS); }
     tc::mbar_init(&sm.qfull, 1);
-    tc::mbar_init(&sm.qconv, LY::EPI_THREADS);
     tc::mbar_init(&sm.drain, 1);
     sm.abort = 0;
     tc::fence_mbar_init();
   }
   for (int i = tid; i < QPB * HH; i += kThreads) {
     const int qi = i / HH, h = i % HH;
-    sm.wsm[qi][h] = qi < nq ? a.w[(static_cast<size_t>(b) * a.T + t0 + qi) * HH + h] : 0.0f;
+    const size_t wi = (static_cast<size_t>(b) * a.T + t0 + qi) * HH + h;
+    // e4m3 q: its positive per-(row, head) scale moves through the ReLU into w
+    sm.wsm[qi][h] = qi < nq ? (FP8 ? a.w[wi] * a.qscale[wi] : a.w[wi]) : 0.0f;
   }
   if (warp == 1) {
     tc::tmem_alloc(&sm.tmem_base, TMEM_COLS);
@@ -207,17 +214,26 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
       const int qrow = (b * a.T + t0) * HH;
       // q rows are read by this CTA only; key tiles by every CTA of the sequence
       const uint64_t once = tc::l2_evict_first(), keep = tc::l2_evict_last();
-      tc::mbar_arrive_expect_tx(&sm.qfull, 2 * NCOL * 128);
-      tc::tma_load_2d_hint(sm.qb[0], &tm_q, &sm.qfull, 0, qrow, once);
-      tc::tma_load_2d_hint(sm.qb[1], &tm_q, &sm.qfull, 64, qrow, once);
-      const int krow0 = b * a.S_cap;
+      if (FP8) {
+        // 256 q rows of 128 e4m3 bytes: one 128-byte-swizzled box
+        tc::mbar_arrive_expect_tx(&sm.qfull, NCOL * 128);
+        tc::tma_load_2d_hint(sm.qb[0], &tm_q, &sm.qfull, 0, qrow, once);
+      } else {
+        tc::mbar_arrive_expect_tx(&sm.qfull, 2 * NCOL * 128);
+        tc::tma_load_2d_hint(sm.qb[0], &tm_q, &sm.qfull, 0, qrow, once);
+        tc::tma_load_2d_hint(sm.qb[1], &tm_q, &sm.qfull, 64, qrow, once);
+      }
+      const int krow0 = b * key_rows;
+      // stages: bf16 keys two K-halves of 64 features per tile, e4m3 keys the whole tile
+      constexpr int kPerTile = FP8 ? 1 : 2;
       int issued = 0;
-      for (int it = 0; !E4M3 && it < 2 * nt; ++it) {
+      for (int it = 0; it < kPerTile * nt; ++it) {
         const int s = it % KSTAGES;
         const uint32_t ph = (it / KSTAGES) & 1;
         if (!tc::mbar_wait(&sm.empty[s], ph ^ 1, &sm.abort, lim)) { set_abort(sm, status); break; }
         tc::mbar_arrive_expect_tx(&sm.full[s], KT * 128);
-        tc::tma_load_2d_hint(sm.kst[s], &tm_k, &sm.full[s], (it & 1) * 64, krow0 + (it >> 1) * KT, keep);
+        if (FP8) tc::tma_load_2d_hint(sm.kst[s], &tm_k, &sm.full[s], 0, krow0 + it * KT, keep);
+        else tc::tma_load_2d_hint(sm.kst[s], &tm_k, &sm.full[s], (it & 1) * 64, krow0 + (it >> 1) * KT, keep);
         issued = it + 1;
       }
       // no copy of ours may still be landing in shared memory when the CTA exits
@@ -229,7 +245,7 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
   } else if (warp == 1) {
     // ================= MMA issuer =================
     if (lane == 0) {
-      bool ok = tc::mbar_wait(E4M3 ? &sm.qconv : &sm.qfull, 0, &sm.abort, lim);
+      bool ok = tc::mbar_wait(&sm.qfull, 0, &sm.abort, lim);
       if (!ok) set_abort(sm, status);
       const uint32_t qb0 = tc::smem_u32(sm.qb[0]);
       const uint32_t qb1 = tc::smem_u32(sm.qb[1]);
@@ -238,17 +254,23 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
         if (!tc::mbar_wait(&sm.tempty[acc], ((j >> 1) & 1) ^ 1, &sm.abort, lim)) { set_abort(sm, status); break; }
         tc::tc_fence_after();
         const uint32_t d_tmem = tmem + acc * NCOL;
-        for (int h = 0; h < 2; ++h) {
-          const int it = 2 * j + h;
+        for (int h = 0; h < (FP8 ? 1 : 2); ++h) {
+          const int it = FP8 ? j : 2 * j + h;
           const int s = it % KSTAGES;
           if (!tc::mbar_wait(&sm.full[s], (it / KSTAGES) & 1, &sm.abort, lim)) { set_abort(sm, status); ok = false; break; }
           tc::tc_fence_after();
           const uint32_t a_base = tc::smem_u32(sm.kst[s]);
           const uint32_t b_base = h ? qb1 : qb0;
+          // each MMA takes 32 bytes of every 128-byte row: 16 bf16 or 32 e4m3 features
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc::mma_f16(d_tmem, tc::sdesc_k_sw128(a_base + kk * 32), tc::sdesc_k_sw128(b_base + kk * 32),
-                        E4M3 ? IDESC_F16 : IDESC, (h | kk) != 0);
+          for (int kk = 0; kk < 4; ++kk) {
+            if (FP8)
+              tc::mma_f8f6f4(d_tmem, tc::sdesc_k_sw128(a_base + kk * 32), tc::sdesc_k_sw128(b_base + kk * 32),
+                             IDESC_E4M3, kk != 0);
+            else
+              tc::mma_f16(d_tmem, tc::sdesc_k_sw128(a_base + kk * 32), tc::sdesc_k_sw128(b_base + kk * 32),
+                          IDESC, (h | kk) != 0);
+          }
           tc::mma_commit(&sm.empty[s]);   // frees the stage once these MMAs are done
         }
         if (!ok) break;
@@ -259,62 +281,6 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
       if (!tc::mbar_wait(&sm.drain, 0, nullptr, 4000000000ull)) set_abort(sm, status);
     }
     __syncwarp();
-  } else if (warp >= LY::CONV_WARP0) {
-    // ================= e4m3 keys -> f16 operand tiles =================
-    if constexpr (E4M3) {
-      const int ct = tid - LY::CONV_WARP0 * 32;     // 0..63
-      const uint8_t* kbase = static_cast<const uint8_t*>(a.kI);
-      const long long krow0 = static_cast<long long>(b) * a.S_cap;
-      const long long nrows = static_cast<long long>(a.B) * a.S_cap;
-      // a tile is 128 rows x 128 B = 1024 pieces of 16 B; piece c = ct + 64u:
-      // row c >> 3, features 16 (c & 7) .. +15 (a warp reads 4 whole rows)
-      auto load_tile = [&](int j, uint4 (&raw)[16]) {
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int c = ct + 64 * u;
-          const long long row = krow0 + static_cast<long long>(j) * KT + (c >> 3);
-          raw[u] = row < nrows ? __ldg(reinterpret_cast<const uint4*>(kbase + row * DD + 16 * (c & 7)))
-                               : make_uint4(0u, 0u, 0u, 0u);
-        }
-      };
-      // both K-halves of tile j go to ring stages 2j, 2j+1
-      auto store_tile = [&](int j, const uint4 (&raw)[16]) -> bool {
-        const int it0 = 2 * j;
-        const int s0 = it0 % KSTAGES, s1 = (it0 + 1) % KSTAGES;
-        if (!tc::mbar_wait(&sm.empty[s0], ((it0 / KSTAGES) & 1) ^ 1, &sm.abort, lim)) return false;
-        if (!tc::mbar_wait(&sm.empty[s1], (((it0 + 1) / KSTAGES) & 1) ^ 1, &sm.abort, lim)) return false;
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const int c = ct + 64 * u;
-          const int r = c >> 3, pc = c & 7;
-          uint8_t* dst = sm.kst[pc < 4 ? s0 : s1] + r * 128;
-          const int c0 = 2 * (pc & 3);                // f16 chunks c0, c0+1 of the 64-feature half
-          const uint4 x = raw[u];
-          const uint4 o0 = make_uint4(e4m3x2_to_f16x2(x.x), e4m3x2_to_f16x2(x.x >> 16), e4m3x2_to_f16x2(x.y),
-                                      e4m3x2_to_f16x2(x.y >> 16));
-          const uint4 o1 = make_uint4(e4m3x2_to_f16x2(x.z), e4m3x2_to_f16x2(x.z >> 16), e4m3x2_to_f16x2(x.w),
-                                      e4m3x2_to_f16x2(x.w >> 16));
-          *reinterpret_cast<uint4*>(dst + ((c0 ^ (r & 7)) << 4)) = o0;
-          *reinterpret_cast<uint4*>(dst + (((c0 + 1) ^ (r & 7)) << 4)) = o1;
-        }
-        tc::fence_proxy_async_smem();
-        tc::mbar_arrive(&sm.full[s0]);
-        tc::mbar_arrive(&sm.full[s1]);
-        return true;
-      };
-      // one tile's loads stay in flight while the previous one is converted
-      uint4 ra[16], rb[16];
-      bool ok = true;
-      load_tile(0, ra);
-      for (int j = 0; j < nt; j += 2) {
-        if (j + 1 < nt) load_tile(j + 1, rb);
-        if (!(ok = store_tile(j, ra))) break;
-        if (j + 1 >= nt) break;
-        if (j + 2 < nt) load_tile(j + 2, ra);
-        if (!(ok = store_tile(j + 1, rb))) break;
-      }
-      if (!ok) set_abort(sm, status);
-    }
   } else {
     // ================= epilogue: scores + streaming top-k =================
     const int wg = (warp - 2) >> 2;               // epilogue warpgroup
@@ -332,46 +298,6 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
 #pragma unroll
     for (int qq = 0; qq < RPW; ++qq) { cnt[qq] = 0; tau[qq] = 0u; rmin[qq] = 0xFFFFFFFFu; rmax[qq] = 0u; }
 
-    if constexpr (E4M3) {
-      // this warpgroup's two q rows: thread = (row q0 + wtid / 64, head wtid % 64)
-      const bool okq = tc::mbar_wait(&sm.qfull, 0, &sm.abort, lim);
-      if (!okq) set_abort(sm, status);
-      const int qi = q0 + (wtid >> 6), hd = wtid & 63;
-      const int qr = qi * HH + hd;                  // row of the 256-row B operand
-      const int sw = qr & 7;
-      float amax = 0.0f;
-      if (okq) {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            float f[8];
-            bf16x8_to_f32(*reinterpret_cast<const uint4*>(sm.qb[hh] + qr * 128 + ((c ^ sw) << 4)), f);
-#pragma unroll
-            for (int x = 0; x < 8; ++x) amax = fmaxf(amax, fabsf(f[x]));
-          }
-      }
-      const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
-      const int e = amax > 0.0f ? max(-120, min(126, 141 - ex)) : 0;
-      const float scale = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
-      const float inv_scale = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
-      if (okq) {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint4* p = reinterpret_cast<uint4*>(sm.qb[hh] + qr * 128 + ((c ^ sw) << 4));
-            float f[8];
-            bf16x8_to_f32(*p, f);
-            *p = make_uint4(f32x2_to_f16x2(f[0] * scale, f[1] * scale), f32x2_to_f16x2(f[2] * scale, f[3] * scale),
-                            f32x2_to_f16x2(f[4] * scale, f[5] * scale), f32x2_to_f16x2(f[6] * scale, f[7] * scale));
-          }
-        sm.wsm[qi][hd] *= inv_scale;
-      }
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(&sm.qconv);
-      wsync();                                      // the warpgroup's scaled weights are in place
-    }
     // e4m3: the key scales of the next tile are loaded one tile ahead
     const float* ksrow = E4M3 ? a.kscale + static_cast<size_t>(b) * a.S_cap : nullptr;
     float ks_next = (E4M3 && key_local < n_keys) ? __ldg(ksrow + key_local) : 1.0f;
@@ -510,25 +436,61 @@ bool indexer_prefill_tc_supported(const IndexerArgs& a) {
   return a.H == HH && a.D == DD && a.T > kDecodeMaxT && (!a.e4m3 || a.kscale != nullptr);
 }
 
-cudaError_t launch_indexer_prefill_tc(const IndexerArgs& a, int* dev_status, cudaStream_t st) {
+size_t indexer_prefill_tc_ws_bytes(int B, int T, int S, int H, int D, bool e4m3) {
+  // e4m3 keys (with bf16 q) on this kernel's shape: their exact bf16
+  // widening, [B, S, 128]; e4m3 q with e4m3 keys needs none
+  if (!e4m3 || H != HH || D != DD || T <= kDecodeMaxT) return 0;
+  return (static_cast<size_t>(B) * S * DD * 2 + 255) / 256 * 256;
+}
+
+cudaError_t launch_indexer_prefill_tc(const IndexerArgs& a, void* ws, size_t ws_bytes, int* dev_status,
+                                      cudaStream_t st) {
   CUtensorMap tm_q, tm_k;
-  // q as [B*T*H, 128] bf16 rows, box 256 rows; kI as [B*S_cap, 128], box 128 rows
+  if (a.qscale) {
+    // e4m3 q and keys as stored: q as [B*T*H, 128] bytes, box 256 rows; keys
+    // as [B*S_cap, 128] bytes, box 128 rows (128-byte rows, 128-byte swizzle)
+    if (!a.e4m3 || !encode_tmap_2d(&tm_q, a.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                                   static_cast<uint64_t>(a.B) * a.T * HH, DD, NCOL, DD))
+      return cudaErrorInvalidValue;
+    if (!encode_tmap_2d(&tm_k, a.kI, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, static_cast<uint64_t>(a.B) * a.S_cap, DD, KT,
+                        DD))
+      return cudaErrorInvalidValue;
+    const int n_groups = (a.T + QPB - 1) / QPB;
+    const size_t smem = sizeof(TcSmem) + 1024;
+    auto kern = indexer_prefill_tc_kernel<QK_E4M3>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(n_groups, a.B), Layout::NTHREADS, smem, st>>>(tm_q, tm_k, a, n_groups, a.S_cap, dev_status);
+    return cudaGetLastError();
+  }
+  // q as [B*T*H, 128] bf16 rows, box 256 rows; keys as [B*key_rows, 128], box 128 rows
   if (!encode_tmap_2d(&tm_q, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(a.B) * a.T * HH, DD,
                       NCOL, 64))
     return cudaErrorInvalidValue;
-  // e4m3 keys are read with plain loads; the key map is then unused
-  if (a.e4m3) tm_k = tm_q;
-  else if (!encode_tmap_2d(&tm_k, a.kI, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(a.B) * a.S_cap,
-                           DD, KT, 64))
+  const void* keys = a.kI;
+  int key_rows = a.S_cap;
+  if (a.e4m3) {
+    // e4m3 keys are widened to bf16 once per call (exact; the scale stays a
+    // per-key factor applied after the head sum), then fed by TMA like bf16 keys
+    if (ws_bytes < indexer_prefill_tc_ws_bytes(a.B, a.T, a.S, a.H, a.D, true) || ws == nullptr)
+      return cudaErrorInvalidValue;
+    const size_t chunks = static_cast<size_t>(a.B) * a.S * (DD / 16);
+    const int blocks = static_cast<int>(std::min<size_t>((chunks + 255) / 256, 148 * 16));
+    widen_e4m3_keys_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(a.kI), static_cast<uint4*>(ws), a.B,
+                                                   a.S, a.S_cap);
+    keys = ws;
+    key_rows = a.S;
+  }
+  if (!encode_tmap_2d(&tm_k, keys, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(a.B) * key_rows, DD,
+                      KT, 64))
     return cudaErrorInvalidValue;
   const int n_groups = (a.T + QPB - 1) / QPB;
   const size_t smem = sizeof(TcSmem) + 1024;
-  auto kern = a.e4m3 ? indexer_prefill_tc_kernel<true> : indexer_prefill_tc_kernel<false>;
+  auto kern = a.e4m3 ? indexer_prefill_tc_kernel<KEYS_E4M3> : indexer_prefill_tc_kernel<KEYS_BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(n_groups, a.B);
-  kern<<<grid, a.e4m3 ? Layout<true>::NTHREADS : Layout<false>::NTHREADS, smem, st>>>(tm_q, tm_k, a, n_groups,
-                                                                                   dev_status);
+  kern<<<grid, Layout::NTHREADS, smem, st>>>(tm_q, tm_k, a, n_groups, key_rows, dev_status);
   return cudaGetLastError();
 }
 

@@ -7,7 +7,8 @@
 //
 // One CTA per (query row, split).  The CTA walks its share of the index row
 // in chunks of KC positions, gathers those K and V rows into shared memory
-// with 16-byte asynchronous copies (double buffered), and runs a
+// through registers (double buffered: the next chunk's loads are in flight
+// during the current chunk's math), and runs a
 // flash-style online softmax on the tensor cores with the heads on the MMA
 // M axis.  Four warps: two head tiles of 16 x two halves of every chunk; the
 // halves are merged at the end.  With one split the CTA writes bf16 O;
@@ -42,28 +43,47 @@ struct Partial {               // per (row, split): m[HQMAX], l[HQMAX], o[HQMAX]
   __host__ __device__ static size_t floats(int dh) { return (size_t)2 * HQMAX + (size_t)HQMAX * dh; }
 };
 
+// Chunk gathers go through registers: each thread loads its 16-byte pieces
+// of the chunk's K and V rows with plain global loads (the next chunk's are
+// in flight while the current one is computed), then stores them into the
+// shared-memory buffer.  Plain loads sustain several times the random-row
+// gather rate of cp.async on this GPU.
 template <int DH>
-__device__ __forceinline__ void gather_chunk(AttnSmem<DH>& sm, int buf, const int32_t* irow, int j0, int k,
-                                             const __nv_bfloat16* Kb, const __nv_bfloat16* Vb, int S, int tid) {
-  constexpr int CH = DH / 8;
-  // an index outside [0, S) is an empty slot: never dereferenced, masked out
-  if (tid < KC) {
-    const int j = j0 + tid;
-    const int s = j < k ? irow[j] : -1;
-    sm.idx[buf][tid] = (s >= 0 && s < S) ? s : -1;
-  }
-  // each thread reads the index itself (the smem copy is for the score mask)
-  for (int i = tid; i < KC * CH * 2; i += ATHREADS) {
-    const int which = i / (KC * CH);            // 0: K, 1: V
-    const int r = (i / CH) % KC, c = i % CH;
+struct ChunkRegs {
+  static constexpr int CH = DH / 8;                 // 16-byte pieces per row
+  static constexpr int N = KC * CH / ATHREADS;      // pieces per thread per tensor
+  uint4 k[N], v[N];
+  int s[N];                                         // source row of each piece (-1: empty slot)
+};
+
+template <int DH>
+__device__ __forceinline__ void gather_load(ChunkRegs<DH>& g, const int32_t* irow, int j0, int k,
+                                            const __nv_bfloat16* Kb, const __nv_bfloat16* Vb, int S, int tid) {
+  constexpr int CH = ChunkRegs<DH>::CH;
+#pragma unroll
+  for (int u = 0; u < ChunkRegs<DH>::N; ++u) {
+    const int i = tid + ATHREADS * u;
+    const int r = i / CH, c = i % CH;
     const int j = j0 + r;
-    const int s = j < k ? __ldg(irow + j) : -1;
-    const bool ok = s >= 0 && s < S;
-    const __nv_bfloat16* base = which ? Vb : Kb;
-    __nv_bfloat16* dst = which ? &sm.v[buf][r][c * 8] : &sm.k[buf][r][c * 8];
-    cp_async16(dst, ok ? base + (size_t)s * DH + c * 8 : base, ok);
+    const int src = j < k ? __ldg(irow + j) : -1;
+    const bool ok = src >= 0 && src < S;   // an index outside [0, S) is an empty slot: never read
+    g.s[u] = ok ? src : -1;
+    g.k[u] = ok ? __ldcg(reinterpret_cast<const uint4*>(Kb + (size_t)src * DH) + c) : make_uint4(0u, 0u, 0u, 0u);
+    g.v[u] = ok ? __ldcg(reinterpret_cast<const uint4*>(Vb + (size_t)src * DH) + c) : make_uint4(0u, 0u, 0u, 0u);
   }
-  cp_async_commit();
+}
+
+template <int DH>
+__device__ __forceinline__ void gather_store(AttnSmem<DH>& sm, int buf, const ChunkRegs<DH>& g, int tid) {
+  constexpr int CH = ChunkRegs<DH>::CH;
+#pragma unroll
+  for (int u = 0; u < ChunkRegs<DH>::N; ++u) {
+    const int i = tid + ATHREADS * u;
+    const int r = i / CH, c = i % CH;
+    *reinterpret_cast<uint4*>(&sm.k[buf][r][c * 8]) = g.k[u];
+    *reinterpret_cast<uint4*>(&sm.v[buf][r][c * 8]) = g.v[u];
+    if (c == 0) sm.idx[buf][r] = g.s[u];
+  }
 }
 
 template <int DH>
@@ -98,7 +118,11 @@ sparse_attn_kernel(AttnArgs a, int nsplit, int chunks_per_split, float* partials
   const int c_begin = split * chunks_per_split;
   const int c_end = min(n_chunks_total, c_begin + chunks_per_split);
 
-  if (c_begin < c_end) gather_chunk<DH>(sm, 0, irow, c_begin * KC, a.k, Kb, Vb, a.S, tid);
+  ChunkRegs<DH> gr;
+  if (c_begin < c_end) {
+    gather_load<DH>(gr, irow, c_begin * KC, a.k, Kb, Vb, a.S, tid);
+    gather_store<DH>(sm, 0, gr, tid);
+  }
   cp_async_wait<0>();
   __syncthreads();
 
@@ -122,7 +146,8 @@ sparse_attn_kernel(AttnArgs a, int nsplit, int chunks_per_split, float* partials
 
   for (int c = c_begin; c < c_end; ++c) {
     const int buf = (c - c_begin) & 1;
-    if (c + 1 < c_end) gather_chunk<DH>(sm, buf ^ 1, irow, (c + 1) * KC, a.k, Kb, Vb, a.S, tid);
+    // the next chunk's loads are in flight while this one is computed
+    if (c + 1 < c_end) gather_load<DH>(gr, irow, (c + 1) * KC, a.k, Kb, Vb, a.S, tid);
     if (active) {
       // scores for this warp's 32 keys of the chunk: 4 n-tiles of 8 keys
       float s[4][4];
@@ -206,7 +231,7 @@ sparse_attn_kernel(AttnArgs a, int nsplit, int chunks_per_split, float* partials
         }
       }
     }
-    cp_async_wait<0>();
+    if (c + 1 < c_end) gather_store<DH>(sm, buf ^ 1, gr, tid);
     __syncthreads();
   }
 

@@ -123,6 +123,37 @@ def make_indexer_inputs(cfg: StackConfig, layer: int, base_seed: int, device, T:
     return q, kI, kscale, w
 
 
+def make_fp8_indexer_inputs(cfg: StackConfig, layer: int, base_seed: int, device, T: int | None = None,
+                            S: int | None = None, t0: int = 0, codes: bool = False):
+    """Indexer inputs with e4m3 queries AND keys: q8 [B,T,H,D] e4m3, q_scale
+    [B,T,H] fp32, k8 [B,S,D] e4m3, k_scale [B,S] fp32, w [B,T,H] fp32.
+
+    Default: the same draws as ``make_indexer_inputs``, each query head and
+    key row stored as e4m3 with scale amax/448.  ``codes``: q and k are the
+    integers {-2..2} (exact e4m3 codes) with power-of-two scales in
+    [2^-3, 2^3], so every score is exact in fp32."""
+    T = cfg.T if T is None else T
+    S = cfg.S if S is None else S
+    s0 = base_seed + 1000 * layer
+    std_q = 1.0 / math.sqrt(cfg.D)
+    std_w = 1.0 / math.sqrt(cfg.H)
+    if codes:
+        q = _draw((cfg.B, T, cfg.H, cfg.D), "int", 1.0, s0 + TID_Q + 100 * t0, device)
+        kf = _draw((cfg.B, S, cfg.D), "int", 1.0, s0 + TID_KI, device)
+        w = _draw((cfg.B, T, cfg.H), "int", 1.0, s0 + TID_W + 100 * t0, device)
+        gq = _gen(device, s0 + 77 + 100 * t0)
+        gk = _gen(device, s0 + 78)
+        q_scale = torch.pow(2.0, torch.randint(-3, 4, (cfg.B, T, cfg.H), generator=gq, device=device).float())
+        k_scale = torch.pow(2.0, torch.randint(-3, 4, (cfg.B, S), generator=gk, device=device).float())
+        return q.to(torch.float8_e4m3fn), q_scale, kf.to(torch.float8_e4m3fn), k_scale, w
+    q = _draw((cfg.B, T, cfg.H, cfg.D), cfg.dist, std_q, s0 + TID_Q + 100 * t0, device)
+    w = _draw((cfg.B, T, cfg.H), cfg.dist, std_w, s0 + TID_W + 100 * t0, device)
+    kf = _draw((cfg.B, S, cfg.D), cfg.dist, std_q, s0 + TID_KI, device)
+    q8, q_scale = quantize_e4m3(q)
+    k8, k_scale = quantize_e4m3(kf)
+    return q8, q_scale, k8, k_scale, w
+
+
 def make_attn_inputs(cfg: StackConfig, layer: int, base_seed: int, device, T: int | None = None,
                      S: int | None = None, t0: int = 0):
     """Q [B,T,Hq,Dh], K [B,S,Dh], V [B,S,Dh], all bf16."""

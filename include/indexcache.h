@@ -106,7 +106,8 @@ size_t ic_workspace_size(const ic_dims* dims);
  *
  * k_scale must be NULL for IC_BF16 (factor 1) and non-NULL for IC_E4M3.
  * The L x L scores are never written to memory on the prefill path; rows with
- * few queries per sequence (decode) stage one score row per query in `ws`.
+ * few queries per sequence (decode) stage one score row per query in `ws`,
+ * and e4m3 keys on the prefill path take their exact bf16 widening there.
  * Errors: IC_ERR_ARG (pointers, sizes, q_pos0 + T > S, S > S_cap, workspace
  * smaller than ic_workspace_size), IC_ERR_UNSUPPORTED (H > 64, D not in
  * {32,64,128}, k > 2048), IC_ERR_CUDA. */
@@ -114,6 +115,23 @@ ic_status ic_indexer_topk(int B, int T, int S, int S_cap, int H, int D, int k, i
                           const void* q, const void* kI, int k_dtype, const float* k_scale,
                           const float* w, int32_t* idx_out, void* ws, size_t ws_bytes,
                           void* stream);
+
+/* ic_indexer_topk with fp8 queries and keys (e4m3, as stored), for the
+ * tensor-core fp8 rate (notes page, "背景 & 问题提出": the indexer is the
+ * O(L^2) term; DSA's lightning indexer runs in low precision):
+ *
+ *   I[b,t,s] = sum_h w[b,t,h] * ReLU( q_scale[b,t,h] * (q8[b,t,h,:] . kI8[b,s,:]) * k_scale[b,s] )
+ *
+ * q [B,T,H,D] e4m3 bytes, q_scale [B,T,H] fp32 > 0, kI [B,S_cap,D] e4m3
+ * bytes, k_scale [B,S_cap] fp32 > 0; the rest as for ic_indexer_topk.  The
+ * scales are positive, so both leave the ReLU: the kernel multiplies w by
+ * q_scale and the head sum by k_scale, and the tensor cores take the e4m3
+ * bytes as stored (kind::f8f6f4).  No workspace.
+ * Errors: as ic_indexer_topk; IC_ERR_UNSUPPORTED unless H = 64, D = 128 and
+ * T > 8 (prefill rows). */
+ic_status ic_indexer_topk_fp8(int B, int T, int S, int S_cap, int H, int D, int k, int q_pos0,
+                              const void* q, const float* q_scale, const void* kI, const float* k_scale,
+                              const float* w, int32_t* idx_out, void* stream);
 
 /* Sparse core attention over selected rows (notes page, "背景 & 问题提出":
  * core attention only on the k selected tokens):

@@ -11,6 +11,7 @@ computes every step in float64 with NumPy.
 from .indexcache import (  # noqa: F401
     bf16_to_f64,
     e4m3_to_f64,
+    dequantize_e4m3,
     indexer_scores,
     topk_positions,
     indexer_topk,

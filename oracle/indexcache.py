@@ -83,6 +83,13 @@ def e4m3_to_f64(bits) -> np.ndarray:
     return np.where((e == 15) & (m == 7), np.nan, out)
 
 
+def dequantize_e4m3(bits, scale) -> np.ndarray:
+    """e4m3 codes times their positive scale, one scale per vector of the
+    last axis (a key row, or a query head): the value the fp8 inputs stand
+    for, exactly, in float64."""
+    return e4m3_to_f64(bits) * np.asarray(scale, dtype=np.float64)[..., None]
+
+
 # ---------------------------------------------------------------------------
 # Step C2: indexer scores.
 # ---------------------------------------------------------------------------

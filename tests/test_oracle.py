@@ -231,6 +231,22 @@ def test_e4m3_decode_all_codes():
     assert ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9
 
 
+def test_e4m3_dequantise_closed_form():
+    # codes of 1, -2, 0.5 and the smallest subnormal 2^-9, one scale per row
+    codes = np.array([[0x38, 0xC0, 0x30, 0x01], [0x38, 0xC0, 0x30, 0x01]], dtype=np.uint8)
+    scale = np.array([0.25, 8.0])
+    want = np.array([[0.25, -0.5, 0.125, 2.0 ** -11], [8.0, -16.0, 4.0, 2.0 ** -6]])
+    assert np.array_equal(oracle.dequantize_e4m3(codes, scale), want)
+    # a scale per query head of a [T, H, D] tensor broadcasts over D only
+    rng = np.random.default_rng(4)
+    c = rng.integers(0, 256, (3, 5, 7)).astype(np.uint8)
+    c[c == 0x7F] = 0x7E
+    c[c == 0xFF] = 0xFE
+    sc = rng.uniform(0.1, 4.0, (3, 5))
+    ref = torch.from_numpy(c).view(torch.float8_e4m3fn).to(torch.float64).numpy() * sc[..., None]
+    assert np.array_equal(oracle.dequantize_e4m3(c, sc), ref)
+
+
 # ---------------------------------------------------------------------------
 # Sparse attention (C5).
 # ---------------------------------------------------------------------------
