@@ -10,8 +10,8 @@
 //
 // Every query row gathers its own k K rows and k V rows, so the work per row
 // is a pair of skinny products over gathered operands; the bound is the
-// gather out of L2 (512 B per selected row).  Keys go on the MMA M axis (128
-// per tile, TMEM lanes):
+// gather out of L2, and the design keeps as many gathered bytes in flight as
+// shared memory allows.  Keys go on the MMA M axis (128 per tile, TMEM lanes):
 //
 //   S^T[key, h]  = K_tile (M=128 keys, K-major) x Q^T (N=32 heads, K-major)
 //   O^T[d, h]   += V_tile^T (M=128 d, MN-major) x P^T (N=32 heads, MN-major)
@@ -20,25 +20,35 @@
 // scores, and the output accumulates in TMEM with d on the lanes.
 //
 // Persistent CTAs (one per SM) walk query rows row = blockIdx.x + i*gridDim.x.
-// Warp roles (18 warps):
+// Warp roles (14 warps):
 //   warps 0-7  softmax + epilogue in two head groups: warps 0-3 own heads
 //              0-15, warps 4-7 heads 16-31 (warp w reads TMEM lane quarter
 //              w % 4); thread = key lane for P, = d lane for O.  Thread 0
 //              also loads Q (TMA tile) and the index row (bulk copy) two
 //              rows ahead into a double buffer.
 //   warp 8     MMA issuer of QK^T, over the CTA's tiles in one flat sequence
-//   warp 9     MMA issuer of PV (tile g after its P is written); two issuing
+//   warp 13    MMA issuer of PV (tile g after its P is written); two issuing
 //              threads, because the issue of a tcgen05.mma holds its thread
 //              about as long as one of these N = 32 MMAs runs
-//   warps 10-17 producers: the K rows and the V rows of every tile, gathered
-//              with 16-byte global loads into registers and stored into a
-//              ring of 32 KB slots (order K0 V0 K1 V1 ...) in the
-//              128-byte-swizzled operand layout.  Every producer thread moves
-//              one 16-byte chunk of an eighth of the rows of every slot and
-//              keeps the next slot's loads in flight while it stores one.
-//              (Measured on B300: random 256-byte rows out of L2 reach about
-//              5 TB/s through cp.async and about 14-18 TB/s through plain
-//              loads into registers.)
+//   warps 9-12 producers: the K rows and the V rows of every tile, gathered
+//              with 16-byte asynchronous copies into a ring of 32 KB slots
+//              (order K0 V0 K1 V1 ...) in the 128-byte-swizzled operand layout.
+//              Every producer thread copies one 16-byte chunk of an eighth of
+//              the rows of every slot; a slot is published (the threads' own
+//              copies waited for and fenced into the async proxy) once LAG
+//              later slots have been issued, so LAG + 1 slots are in flight.
+//              Measured on B300 at L = 32768: four producer warps instead of
+//              two take a layer from 4.17 to 3.94 ms (the producers' own
+//              instruction stream, address arithmetic per 16-byte copy, is
+//              on the critical path).
+//
+// Empty slots (index -1 or outside [0, S)) are masked in the softmax, so
+// their rows may hold anything; they are copied from row (slot position &
+// smask), a readable row that differs from slot to slot.  Copying all of
+// them from one row made every CTA hit the same L2 lines during the
+// early rows (fewer than k causal keys) and slowed the whole launch: 5.02
+// against 4.17 ms per layer at L = 32768.  A zero-filling copy, or an integer
+// modulo per slot, cost more than it saved.
 //
 // Softmax (per head group, the groups never wait on each other): the
 // reference max m_h of a head is raised only when some score of a tile
@@ -74,13 +84,13 @@ constexpr int HG = 16;                       // heads per softmax group
 constexpr int SOFT_THREADS = 256;            // two groups of 128
 constexpr int GROUP_THREADS = 128;
 constexpr int MMA_WARP = 8;
-constexpr int PV_WARP = 9;
-constexpr int PROD_WARP0 = 10;
-constexpr int PROD_WARPS = 8;
+constexpr int PROD_WARP0 = 9;
+constexpr int PROD_WARPS = 4;
 constexpr int PROD_THREADS = PROD_WARPS * 32;
-constexpr int RSTEP = PROD_THREADS / 16;              // rows between a producer thread's rows
 constexpr int PROD_ROWS = KT * 16 / PROD_THREADS;   // rows of a slot each producer thread copies (one chunk each)
-constexpr int NTHREADS = (PROD_WARP0 + PROD_WARPS) * 32;
+constexpr int LAG = 2;                       // slots issued after a slot before it is published
+constexpr int PV_WARP = PROD_WARP0 + PROD_WARPS;   // 11
+constexpr int NTHREADS = (PV_WARP + 1) * 32;
 constexpr uint32_t TMEM_COLS = 128;          // S: 2 x 32 columns, O: 2 x 32 columns
 constexpr float kTau = 8.0f;
 constexpr float kMInit = -1.0e30f;           // reference max before any valid key (finite: no inf - inf)
@@ -102,7 +112,7 @@ struct __align__(1024) AttnTcSmem {
   uint64_t sfull[2], sempty[2];
   uint64_t pfull[2], pempty[2];
   uint64_t ofull[2], oempty[2];
-  uint64_t rowfree[2];                       // both softmax groups are done with a row buffer
+  uint64_t rowfree[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -134,15 +144,12 @@ __device__ __forceinline__ float warp_reduce_scatter16(float (&v)[16], int lane)
 }
 
 // Q rows and the index row of `row` into buffer qb (completion on qfull[qb]).
-// Q and the index row are read once: evict-first, so they do not push the
-// gathered K/V rows out of L2.
 __device__ __forceinline__ void load_row_inputs(AttnTcSmem& sm, const CUtensorMap* tm_q, const AttnArgs& a, int row,
                                                 int qb) {
-  const uint64_t pol = tc::l2_evict_first();
   tc::mbar_arrive_expect_tx(&sm.qfull[qb], Q_BYTES + a.k * 4);
-  tc::tma_load_2d_hint(sm.qs[qb], tm_q, &sm.qfull[qb], 0, row * HQ, pol);
-  tc::tma_load_2d_hint(sm.qs[qb] + Q_BYTES / 2, tm_q, &sm.qfull[qb], 64, row * HQ, pol);
-  tc::bulk_g2s_hint(sm.idx[qb], a.idx + static_cast<size_t>(row) * a.k, a.k * 4, &sm.qfull[qb], pol);
+  tc::tma_load_2d(sm.qs[qb], tm_q, &sm.qfull[qb], 0, row * HQ);
+  tc::tma_load_2d(sm.qs[qb] + Q_BYTES / 2, tm_q, &sm.qfull[qb], 64, row * HQ);
+  tc::bulk_g2s(sm.idx[qb], a.idx + static_cast<size_t>(row) * a.k, a.k * 4, &sm.qfull[qb]);
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -161,6 +168,8 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                          ? (rows - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
                          : 0;
   const uint32_t n_tiles = static_cast<uint32_t>(n_rows) * nt;
+  // rows 0 .. smask are readable (smask + 1 is the largest power of two <= S)
+  const int smask = static_cast<int>((0x80000000u >> __clz(static_cast<uint32_t>(a.S))) - 1u);
 
   if (tid == 0) {
     for (int s = 0; s < NSLOT; ++s) {
@@ -225,72 +234,55 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     __syncwarp();
   } else if (warp >= PROD_WARP0) {
     // ================= producers =================
-    // Item it is K (even) or V (odd) of tile it / 2.  A thread owns 16-byte
-    // chunk c of rows r0, r0 + RSTEP, ... of every item; its loads go to
-    // registers (plain global loads sustain about three times the L2 gather
-    // rate of cp.async here), then into the slot in the operand layout.  The
-    // loads of item it + 1 are in flight while item it is stored.
+    constexpr int RSTEP = PROD_THREADS / 16;
     const int pt = tid - PROD_WARP0 * 32;            // 0 .. PROD_THREADS-1
     const int c = pt & 15;                           // 16-byte chunk of a 256-byte row
     const int half = c >> 3, cc = c & 7;
     const int r0 = pt >> 4;                          // rows r0, r0 + RSTEP, ...
-    const uint4* Kg = reinterpret_cast<const uint4*>(a.K) + c;
-    const uint4* Vg = reinterpret_cast<const uint4*>(a.V) + c;
-    const uint32_t n_items = 2u * n_tiles;
-    const uint64_t keep = tc::l2_evict_last();       // K/V rows are re-read by many rows
-    uint4 buf[2][PROD_ROWS];
-    int sidx[PROD_ROWS];                             // source rows of the current tile (-1: empty slot)
-    size_t base_row = 0;
+    const __nv_bfloat16* Kg = reinterpret_cast<const __nv_bfloat16*>(a.K) + c * 8;
+    const __nv_bfloat16* Vg = reinterpret_cast<const __nv_bfloat16*>(a.V) + c * 8;
+    uint32_t it = 0;
     bool ok = true;
-    // loads of item it into registers; K items (even) first fetch the tile's
-    // index entries, which the tile's V item reuses.  No ring slot is held
-    // while the loads are in flight.
-    auto issue = [&](uint32_t it, uint4 (&b)[PROD_ROWS]) -> bool {
-      if ((it & 1) == 0) {
-        const uint32_t tile = it >> 1;
-        const int n = static_cast<int>(tile / nt);
-        const int j = static_cast<int>(tile % nt);
-        const int qb = n & 1;
-        if (j == 0 && !tc::mbar_wait(&sm.qfull[qb], (n >> 1) & 1, &sm.abort)) return false;
-        const int row = static_cast<int>(blockIdx.x) + n * static_cast<int>(gridDim.x);
-        base_row = static_cast<size_t>(row / a.T) * a.S_cap;
+    for (int n = 0; ok && n < n_rows; ++n) {
+      const int row = static_cast<int>(blockIdx.x) + n * static_cast<int>(gridDim.x);
+      const int qb = n & 1;
+      if (!tc::mbar_wait(&sm.qfull[qb], (n >> 1) & 1, &sm.abort)) { ok = false; break; }
+      const size_t base_row = static_cast<size_t>(row / a.T) * a.S_cap;
+      for (int j = 0; ok && j < nt; ++j) {
+        int src[PROD_ROWS];
         const int32_t* irow = sm.idx[qb] + j * KT;
         const int lim = k - j * KT;                  // positions past k are empty slots
 #pragma unroll
         for (int i = 0; i < PROD_ROWS; ++i) {
           const int r = r0 + RSTEP * i;
           const int s = r < lim ? irow[r] : -1;
-          sidx[i] = (s >= 0 && s < a.S) ? s : -1;
+          src[i] = (s >= 0 && s < a.S) ? s : ((j * KT + r) & smask);   // empty slot: a spread, readable row
+        }
+#pragma unroll 1
+        for (int kv = 0; kv < 2; ++kv, ++it) {
+          const int slot = static_cast<int>(it % NSLOT);
+          if (!tc::mbar_wait(&sm.empty[slot], ((it / NSLOT) & 1) ^ 1, &sm.abort)) { ok = false; break; }
+          const __nv_bfloat16* base = (kv ? Vg : Kg) + base_row * DH;
+          uint8_t* dst = sm.ring[slot] + half * HALF_BYTES;
+#pragma unroll
+          for (int i = 0; i < PROD_ROWS; ++i) {
+            const int r = r0 + RSTEP * i;
+            cp_async16(dst + r * 128 + ((cc ^ (r & 7)) << 4), base + static_cast<size_t>(src[i]) * DH, true);
+          }
+          cp_async_commit();
+          if (it >= LAG) {
+            // the slot issued LAG slots ago has landed: publish it to the tensor core
+            cp_async_wait<LAG>();
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(&sm.full[(it - LAG) % NSLOT]);
+          }
         }
       }
-      const uint4* g = ((it & 1) ? Vg : Kg) + base_row * (DH / 8);
-#pragma unroll
-      for (int i = 0; i < PROD_ROWS; ++i)
-        b[i] = sidx[i] >= 0 ? tc::ldg16_hint(g + static_cast<size_t>(sidx[i]) * (DH / 8), keep)
-                            : make_uint4(0u, 0u, 0u, 0u);
-      return true;
-    };
-    // the ring slot is taken only when the data is about to be written
-    auto store = [&](uint32_t it, const uint4 (&b)[PROD_ROWS]) -> bool {
-      if (!tc::mbar_wait(&sm.empty[it % NSLOT], ((it / NSLOT) & 1) ^ 1, &sm.abort)) return false;
-      uint8_t* dst = sm.ring[it % NSLOT] + half * HALF_BYTES;
-#pragma unroll
-      for (int i = 0; i < PROD_ROWS; ++i) {
-        const int r = r0 + RSTEP * i;
-        *reinterpret_cast<uint4*>(dst + r * 128 + ((cc ^ (r & 7)) << 4)) = b[i];
-      }
-      tc::fence_proxy_async_smem();
-      tc::mbar_arrive(&sm.full[it % NSLOT]);
-      return true;
-    };
-    if (n_items > 0) ok = issue(0, buf[0]);
-    for (uint32_t it = 0; ok && it < n_items; it += 2) {
-      // item it (K) is in buf[0]; item it + 1 (V of the same tile) always exists
-      if (!(ok = issue(it + 1, buf[1]))) break;
-      if (!(ok = store(it, buf[0]))) break;
-      if (it + 2 < n_items && !(ok = issue(it + 2, buf[0]))) break;
-      if (!(ok = store(it + 1, buf[1]))) break;
     }
+    // publish (or, after an abort, just wait out) the last slots in flight
+    cp_async_wait<0>();
+    tc::fence_proxy_async_smem();
+    for (uint32_t i = (it > LAG ? it - LAG : 0); i < it; ++i) tc::mbar_arrive(&sm.full[i % NSLOT]);
     if (!ok) set_abort(sm, status);
   } else if (warp == MMA_WARP) {
     // ================= MMA issuer: S^T = K Q^T =================
@@ -460,11 +452,9 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       tc::tmem_wait_ld();
       tc::tc_fence_before();
       tc::mbar_arrive(&sm.oempty[qb]);
-      // Q and the index row of row n are no longer read by anyone once both
-      // groups passed their last tile (the MMA's last QK^T of the row is then
-      // complete, the producers are past the row): load row n + 2 into the
-      // buffer.  An mbarrier, not a named barrier, so that a group that gave
-      // up never leaves the other one waiting.
+      // Q and the index row of row n are no longer read by anyone (both groups
+      // passed their last tile, the MMA's last QK^T of the row is complete):
+      // load row n + 2 into the buffer
       tc::mbar_arrive(&sm.rowfree[qb]);
       if (tid == 0 && n + 2 < n_rows) {
         if (tc::mbar_wait(&sm.rowfree[qb], (n >> 1) & 1, &sm.abort)) {
@@ -474,15 +464,12 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       }
       __nv_bfloat16* Ob = reinterpret_cast<__nv_bfloat16*>(a.O) + static_cast<size_t>(row) * HQ * DH +
                           static_cast<size_t>(h0) * DH + my_lane;
-      const uint64_t once = tc::l2_evict_first();
 #pragma unroll
-      for (int h = 0; h < HG; ++h)
-        tc::stg_b16_hint(Ob + h * DH, __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(o[h]) * sm.inv_l[h0 + h])),
-                         once);
+      for (int h = 0; h < HG; ++h) Ob[h * DH] = __float2bfloat16_rn(__uint_as_float(o[h]) * sm.inv_l[h0 + h]);
     }
     if (!ok) set_abort(sm, status);
-    // no row-input copy of ours may still be landing when the CTA exits: the
-    // last two rows requested (earlier ones were waited for before their
+    // no row-input copy of ours may still be landing when the CTA exits
+    // (the last two rows requested; earlier ones were waited for before their
     // buffer was reused)
     if (tid == 0) {
       for (int r = rows_loaded > 2 ? rows_loaded - 2 : 0; r < rows_loaded; ++r)

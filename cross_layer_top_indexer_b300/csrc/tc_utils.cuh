@@ -123,10 +123,9 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 
 // ------------------------------------------------------------- L2 policies
 //
-// Data that many CTAs re-read (key tiles, gathered K/V rows) is loaded with
-// an evict-last policy; data each CTA touches once (query rows, index rows,
-// outputs) with evict-first, so the streams do not push the re-read data out
-// of L2.
+// Data that many CTAs re-read (the indexer's key tiles) is loaded with an
+// evict-last policy; data one CTA reads once (its query rows) with
+// evict-first, so the stream does not push the re-read data out of L2.
 
 __device__ __forceinline__ uint64_t l2_evict_last() {
   uint64_t p;
@@ -139,19 +138,6 @@ __device__ __forceinline__ uint64_t l2_evict_first() {
   return p;
 }
 
-// 16-byte read-only global load, not allocated in L1, with an L2 policy.
-__device__ __forceinline__ uint4 ldg16_hint(const void* p, uint64_t pol) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p), "l"(pol));
-  return r;
-}
-
-__device__ __forceinline__ void stg_b16_hint(void* p, uint16_t v, uint64_t pol) {
-  asm volatile("st.global.L1::no_allocate.L2::cache_hint.b16 [%0], %1, %2;" ::"l"(p), "h"(v), "l"(pol) : "memory");
-}
-
 // tma_load_2d with an L2 policy.
 __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
                                                  uint64_t pol) {
@@ -159,15 +145,6 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%3, %4}], [%2], %5;"
       ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(pol)
-      : "memory");
-}
-
-// bulk_g2s with an L2 policy.
-__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                              uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
-      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
 
