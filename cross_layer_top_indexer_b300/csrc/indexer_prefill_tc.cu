@@ -99,10 +99,8 @@ struct __align__(1024) TcSmem {
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  // per tile parity, row and key quarter: insert count, largest and smallest inserted key
+  // per tile parity, row and key quarter: insert count
   int xc[2][QPB][4];
-  uint32_t xmax[2][QPB][4];
-  uint32_t xmin[2][QPB][4];
   SelectScratch scr[QPB];
 };
 
@@ -110,6 +108,17 @@ struct WgSync {
   int id;
   __device__ __forceinline__ void operator()() const { tc::named_sync(id, WG_THREADS); }
 };
+
+// Largest of the warpgroup's per-thread values (all 128 threads call it).
+__device__ __forceinline__ uint32_t list_max(uint32_t v, SelectScratch* scr, int wtid, const WgSync& sync) {
+  v = __reduce_max_sync(0xffffffffu, v);
+  if ((wtid & 31) == 0) scr->warp_sums[wtid >> 5] = static_cast<int>(v);
+  sync();
+  const uint32_t m = max(max(static_cast<uint32_t>(scr->warp_sums[0]), static_cast<uint32_t>(scr->warp_sums[1])),
+                         max(static_cast<uint32_t>(scr->warp_sums[2]), static_cast<uint32_t>(scr->warp_sums[3])));
+  sync();
+  return m;
+}
 
 __device__ __forceinline__ void set_abort(TcSmem& sm, int* status) {
   sm.abort = 1;
@@ -293,10 +302,10 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
     const unsigned lanes_below = (1u << lane) - 1u;
     // per-row state, identical in every thread of the warpgroup
     int cnt[RPW];
-    uint32_t tau[RPW];                              // a key enters iff key > tau
-    uint32_t rmin[RPW], rmax[RPW];                  // bounds of the keys in the list
+    uint32_t tau[RPW];                              // a key enters iff key > tau (every listed key is)
+    uint32_t kmax[RPW];                             // largest key this thread listed (bounds the list at a cut)
 #pragma unroll
-    for (int qq = 0; qq < RPW; ++qq) { cnt[qq] = 0; tau[qq] = 0u; rmin[qq] = 0xFFFFFFFFu; rmax[qq] = 0u; }
+    for (int qq = 0; qq < RPW; ++qq) { cnt[qq] = 0; tau[qq] = 0u; kmax[qq] = 0u; }
 
     // e4m3: the key scales of the next tile are loaded one tile ahead
     const float* ksrow = E4M3 ? a.kscale + static_cast<size_t>(b) * a.S_cap : nullptr;
@@ -363,13 +372,8 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
         valid[qq] = qi < nq && s_pos <= pos0 + qi;
         take[qq] = valid[qq] && key[qq] > tau[qq];
         bal[qq] = __ballot_sync(0xffffffffu, take[qq]);
-        const uint32_t mx = __reduce_max_sync(0xffffffffu, take[qq] ? key[qq] : 0u);
-        const uint32_t mn = __reduce_min_sync(0xffffffffu, take[qq] ? key[qq] : 0xFFFFFFFFu);
-        if (lane == 0) {
-          sm.xc[par][qi][quarter] = __popc(bal[qq]);
-          sm.xmax[par][qi][quarter] = mx;
-          sm.xmin[par][qi][quarter] = mn;
-        }
+        if (take[qq]) kmax[qq] = max(kmax[qq], key[qq]);
+        if (lane == 0) sm.xc[par][qi][quarter] = __popc(bal[qq]);
       }
       // the tile's one barrier: the exchange, and one abort decision for the warpgroup
       if (tc::named_sync_or(1 + wg, WG_THREADS, !ok || sm.abort)) { aborted = true; break; }
@@ -380,10 +384,10 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
         if (cnt[qq] + tot > CAP) {
           // the list would overflow: cut it, raise tau, recount this tile's keys
           uint32_t thr;
-          cnt[qq] = cut_list<WG_THREADS, SEG>(sm.cand_k[qi], sm.cand_p[qi], cnt[qq], a.k, CUT_LIMIT, rmin[qq],
-                                              rmax[qq], &sm.scr[wg], wtid, wsync, &thr);
+          cnt[qq] = cut_list<WG_THREADS, SEG>(sm.cand_k[qi], sm.cand_p[qi], cnt[qq], a.k, CUT_LIMIT, tau[qq],
+                                              list_max(kmax[qq], &sm.scr[wg], wtid, wsync), &sm.scr[wg], wtid, wsync,
+                                              &thr);
           tau[qq] = thr;
-          rmin[qq] = thr;
           take[qq] = valid[qq] && key[qq] > tau[qq];
           bal[qq] = __ballot_sync(0xffffffffu, take[qq]);
           if (lane == 0) sm.xc[par][qi][quarter] = __popc(bal[qq]);
@@ -399,10 +403,6 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
           sm.cand_p[qi][slot] = s_pos;
         }
         cnt[qq] += tot;
-        rmax[qq] = max(rmax[qq], max(max(sm.xmax[par][qi][0], sm.xmax[par][qi][1]),
-                                     max(sm.xmax[par][qi][2], sm.xmax[par][qi][3])));
-        rmin[qq] = min(rmin[qq], min(min(sm.xmin[par][qi][0], sm.xmin[par][qi][1]),
-                                     min(sm.xmin[par][qi][2], sm.xmin[par][qi][3])));
       }
     }
     if (!aborted) aborted = tc::named_sync_or(1 + wg, WG_THREADS, sm.abort != 0);
@@ -415,8 +415,8 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
         int c = cnt[qq];
         if (c > a.k) {
           uint32_t thr;
-          c = cut_list<WG_THREADS, SEG>(sm.cand_k[qi], sm.cand_p[qi], c, a.k, a.k, rmin[qq], rmax[qq], &sm.scr[wg],
-                                        wtid, wsync, &thr);
+          c = cut_list<WG_THREADS, SEG>(sm.cand_k[qi], sm.cand_p[qi], c, a.k, a.k, tau[qq],
+                                        list_max(kmax[qq], &sm.scr[wg], wtid, wsync), &sm.scr[wg], wtid, wsync, &thr);
         }
         int32_t* row = out + static_cast<size_t>(qi) * a.k;
         for (int x = wtid; x < a.k; x += WG_THREADS) row[x] = x < c ? sm.cand_p[qi][x] : -1;
