@@ -336,10 +336,16 @@ __global__ void attn_combine_kernel(const float* partials, int nsplit, int Hq, v
   reinterpret_cast<__nv_bfloat16*>(O)[((size_t)row * Hq + h) * DH + d] = __float2bfloat16_rn(v);
 }
 
+// Splits of the k positions of a row: about four chunks per CTA (fewer
+// partial states to write and merge), but at least one CTA per SM in all.
+// Measured at the decode workload (32 rows, k = 2048, 32 chunks): 1, 2, 4, 8
+// and 16 chunks per CTA take 28.0, 21.7, 19.7, 24.9 and 39.8 us.
 int pick_splits(int rows, int k) {
   const int n_chunks = (k + KC - 1) / KC;
   if (rows >= 2 * 148) return 1;
-  int want = (4 * 148 + rows - 1) / rows;
+  const int by_work = (n_chunks + 3) / 4;
+  const int by_sms = (148 + rows - 1) / rows;
+  const int want = by_work > by_sms ? by_work : by_sms;
   return want < n_chunks ? want : n_chunks;
 }
 
