@@ -428,11 +428,12 @@ cudaError_t launch_select(float* scores, size_t pitch, const IndexerArgs& a, cud
 // kDecHistBits bits).  The threshold bin is the bin of the k-th largest key;
 // the entries in and above it are the candidates.
 //   select_chunk_kernel   one CTA per (chunk of CH scores, row): writes the
-//                         positions of its candidates, in order, to the
-//                         chunk's region and their count
-//   select_finish_kernel  one CTA per row: gathers the candidates in chunk
-//                         order (= position order) into shared memory with
-//                         their keys and cuts them to exactly k
+//                         positions of its candidates and their keys, in
+//                         order, to the chunk's region, and their count
+//   select_finish_kernel  one CTA per row: a warp per chunk copies the
+//                         chunk's (position, key) lists, coalesced, into
+//                         shared memory in chunk order (= position order),
+//                         then cuts them to exactly k
 // Rows with more candidates than FCAP take the general radix path.
 // ---------------------------------------------------------------------------
 constexpr int HBINS = 1 << kDecHistBits;
@@ -444,7 +445,8 @@ struct DecWs {
   float* scores;
   int* hist;    // [rows][HBINS]
   int* cnt;     // [rows][nch]
-  int* cand;    // [rows][nch][CH]
+  int* cand;    // [rows][nch][CH]: positions
+  uint32_t* candk;   // [rows][nch][CH]: their keys
   size_t pitch;
   int nch;
 };
@@ -465,6 +467,8 @@ DecWs carve_ws(void* ws, int rows, int S, size_t* total) {
   off += align256(static_cast<size_t>(rows) * d.nch * sizeof(int));
   d.cand = reinterpret_cast<int*>(p + off);
   off += align256(static_cast<size_t>(rows) * d.nch * CH * sizeof(int));
+  d.candk = reinterpret_cast<uint32_t*>(p + off);
+  off += align256(static_cast<size_t>(rows) * d.nch * CH * sizeof(uint32_t));
   *total = off;
   return d;
 }
@@ -495,7 +499,8 @@ __device__ void threshold_bin(const int* h, int k, int* warp_sums, int* s_bsel, 
 }
 
 __global__ void __launch_bounds__(CTHREADS)
-select_chunk_kernel(const float* scores, size_t pitch, const int* hist, int* cnt, int* cand, int nch, int n, int k) {
+select_chunk_kernel(const float* scores, size_t pitch, const int* hist, int* cnt, int* cand, uint32_t* candk, int nch,
+                    int n, int k) {
   __shared__ int warp_sums[32];
   __shared__ int s_bsel, s_ncand;
   const int row = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
@@ -519,9 +524,14 @@ select_chunk_kernel(const float* scores, size_t pitch, const int* hist, int* cnt
   int tot;
   int off = block_exclusive_scan(cl, warp_sums, CTHREADS, tot, tid, BlockSync());
   int* dst = cand + (static_cast<size_t>(row) * nch + c) * CH;
+  uint32_t* dstk = candk + (static_cast<size_t>(row) * nch + c) * CH;
 #pragma unroll
   for (int j = 0; j < 16; ++j)
-    if (f & (1u << j)) dst[off++] = i0 + j;
+    if (f & (1u << j)) {
+      dst[off] = i0 + j;
+      dstk[off] = float_key(v[j]);
+      ++off;
+    }
   if (tid == 0) cnt[static_cast<size_t>(row) * nch + c] = tot;
 }
 
@@ -534,8 +544,8 @@ struct FinishSmem {
 };
 
 __global__ void __launch_bounds__(STHREADS)
-select_finish_kernel(const float* scores, size_t pitch, const int* hist, const int* cnt, const int* cand, int nch,
-                     int32_t* idx, int n, int k) {
+select_finish_kernel(const float* scores, size_t pitch, const int* hist, const int* cnt, const int* cand,
+                     const uint32_t* candk, int nch, int32_t* idx, int n, int k) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   FinishSmem& sm = *reinterpret_cast<FinishSmem*>(smem_raw);
   const int row = blockIdx.x, tid = threadIdx.x;
@@ -568,16 +578,15 @@ select_finish_kernel(const float* scores, size_t pitch, const int* hist, const i
     radix_select_row(sc, n, k, out);
     return;
   }
+  // a warp per chunk: its (position, key) lists are read coalesced, in order
   const int* crand = cand + static_cast<size_t>(row) * nch * CH;
-  for (int i = tid; i < ncand; i += STHREADS) {
-    int lo = 0, hi = nc;                         // largest c with coff[c] <= i
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (sm.coff[mid] <= i) lo = mid; else hi = mid;
+  const uint32_t* crandk = candk + static_cast<size_t>(row) * nch * CH;
+  for (int c = tid >> 5; c < nc; c += SWARPS) {
+    const int base = sm.coff[c], nci = sm.coff[c + 1] - base;
+    for (int i = tid & 31; i < nci; i += 32) {
+      sm.pos[base + i] = crand[static_cast<size_t>(c) * CH + i];
+      sm.key[base + i] = crandk[static_cast<size_t>(c) * CH + i];
     }
-    const int p = crand[static_cast<size_t>(lo) * CH + (i - sm.coff[lo])];
-    sm.pos[i] = p;
-    sm.key[i] = float_key(sc[p]);
   }
   __syncthreads();
   if (ncand > k) {
@@ -592,7 +601,7 @@ cudaError_t launch_chunked_select(const DecWs& d, const IndexerArgs& a, cudaStre
   const int n = a.q_pos0 + 1;                    // one row per sequence (T = 1)
   if (n > a.k) {
     dim3 g1((n + CH - 1) / CH, a.B);
-    select_chunk_kernel<<<g1, CTHREADS, 0, st>>>(d.scores, d.pitch, d.hist, d.cnt, d.cand, d.nch, n, a.k);
+    select_chunk_kernel<<<g1, CTHREADS, 0, st>>>(d.scores, d.pitch, d.hist, d.cnt, d.cand, d.candk, d.nch, n, a.k);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -600,7 +609,8 @@ cudaError_t launch_chunked_select(const DecWs& d, const IndexerArgs& a, cudaStre
   cudaError_t e = cudaFuncSetAttribute(select_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  select_finish_kernel<<<a.B, STHREADS, smem, st>>>(d.scores, d.pitch, d.hist, d.cnt, d.cand, d.nch, a.idx, n, a.k);
+  select_finish_kernel<<<a.B, STHREADS, smem, st>>>(d.scores, d.pitch, d.hist, d.cnt, d.cand, d.candk, d.nch, a.idx,
+                                                     n, a.k);
   return cudaGetLastError();
 }
 
