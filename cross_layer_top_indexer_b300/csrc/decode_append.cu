@@ -46,6 +46,8 @@ __device__ __forceinline__ void copy_row(uint8_t* dst, const uint8_t* src, int b
 }
 
 __global__ void __launch_bounds__(64) decode_append_kernel(const __grid_constant__ AppendParams p) {
+  grid_dep_wait();
+  grid_dep_trigger();
   const AppendLayer& L = p.L[blockIdx.x];
   const size_t b = blockIdx.y;
   const size_t row = b * p.S_cap + p.pos;
@@ -120,8 +122,8 @@ extern "C" __attribute__((visibility("default"))) ic_status ic_decode_append(
       A.ks_src = s.k_scale;
     }
   }
-  ic::decode_append_kernel<<<dim3(n_layers, B), 64, 0, static_cast<cudaStream_t>(stream)>>>(p);
-  const cudaError_t e = cudaGetLastError();
+  const cudaError_t e =
+      ic::launch_pdl(ic::decode_append_kernel, dim3(n_layers, B), dim3(64), 0, static_cast<cudaStream_t>(stream), p);
   if (e != cudaSuccess) return fail_msg(IC_ERR_CUDA, std::string("append launch: ") + cudaGetErrorString(e));
   return IC_OK;
 }

@@ -13,6 +13,32 @@ constexpr int kMaxK = 2048;
 constexpr int kDevOk = 0;
 constexpr int kDevTimeout = 1;
 
+// Programmatic dependent launch, used by the decode path's short kernels.  A
+// kernel launched with launch_pdl may start while the kernel before it on the
+// stream is still finishing; before its first access to memory that earlier
+// work writes it calls grid_dep_wait(), which returns once those grids have
+// completed and their writes are visible, and grid_dep_trigger() lets the
+// next such kernel start launching.  In a kernel launched without the
+// attribute both return at once.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Order-preserving map float -> uint32: a > b  <=>  key(a) > key(b).
 // -0.0 is folded onto +0.0 first so that equal scores compare equal.
 __device__ __forceinline__ uint32_t float_key(float f) {

@@ -503,6 +503,8 @@ select_chunk_kernel(const float* scores, size_t pitch, const int* hist, int* cnt
                     int n, int k) {
   __shared__ int warp_sums[32];
   __shared__ int s_bsel, s_ncand;
+  grid_dep_wait();                               // the scores and the histogram of the scorer just before
+  grid_dep_trigger();
   const int row = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
   if (n <= k) return;                            // the finish kernel writes 0 .. n-1
   threshold_bin<CTHREADS>(hist + static_cast<size_t>(row) * HBINS, k, warp_sums, &s_bsel, &s_ncand);
@@ -548,6 +550,8 @@ select_finish_kernel(const float* scores, size_t pitch, const int* hist, const i
                      const uint32_t* candk, int nch, int32_t* idx, int n, int k) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   FinishSmem& sm = *reinterpret_cast<FinishSmem*>(smem_raw);
+  grid_dep_wait();                               // the chunk kernel's lists and counts
+  grid_dep_trigger();
   const int row = blockIdx.x, tid = threadIdx.x;
   const float* sc = scores + static_cast<size_t>(row) * pitch;
   int32_t* out = idx + static_cast<size_t>(row) * k;
@@ -601,17 +605,17 @@ cudaError_t launch_chunked_select(const DecWs& d, const IndexerArgs& a, cudaStre
   const int n = a.q_pos0 + 1;                    // one row per sequence (T = 1)
   if (n > a.k) {
     dim3 g1((n + CH - 1) / CH, a.B);
-    select_chunk_kernel<<<g1, CTHREADS, 0, st>>>(d.scores, d.pitch, d.hist, d.cnt, d.cand, d.candk, d.nch, n, a.k);
-    cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_pdl(select_chunk_kernel, g1, dim3(CTHREADS), 0, st, d.scores, d.pitch,
+                                     static_cast<const int*>(d.hist), d.cnt, d.cand, d.candk, d.nch, n, a.k);
     if (e != cudaSuccess) return e;
   }
   const size_t smem = sizeof(FinishSmem);
   cudaError_t e = cudaFuncSetAttribute(select_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  select_finish_kernel<<<a.B, STHREADS, smem, st>>>(d.scores, d.pitch, d.hist, d.cnt, d.cand, d.candk, d.nch, a.idx,
-                                                     n, a.k);
-  return cudaGetLastError();
+  return launch_pdl(select_finish_kernel, dim3(a.B), dim3(STHREADS), smem, st, static_cast<const float*>(d.scores),
+                    d.pitch, static_cast<const int*>(d.hist), static_cast<const int*>(d.cnt),
+                    static_cast<const int*>(d.cand), static_cast<const uint32_t*>(d.candk), d.nch, a.idx, n, a.k);
 }
 
 template <int D>

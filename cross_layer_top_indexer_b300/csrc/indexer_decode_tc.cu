@@ -160,6 +160,10 @@ indexer_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  // the set-up above may overlap the kernel before; the keys, q, w and scales
+  // are read only once it has completed
+  grid_dep_wait();
+  grid_dep_trigger();
 
   if (warp == 0) {
     // ================= TMA producer =================
@@ -482,8 +486,7 @@ cudaError_t launch_indexer_decode_tc(const IndexerArgs& a, float* scores, size_t
   auto kern = a.e4m3 ? indexer_decode_tc_kernel<true> : indexer_decode_tc_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<grid, NTHREADS, smem, st>>>(tm_q, tm_k, a, scores, pitch, hist, ntile, dev_status);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(grid), dim3(NTHREADS), smem, st, tm_q, tm_k, a, scores, pitch, hist, ntile, dev_status);
 }
 
 }  // namespace ic

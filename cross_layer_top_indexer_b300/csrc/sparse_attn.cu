@@ -93,6 +93,8 @@ sparse_attn_kernel(AttnArgs a, int nsplit, int chunks_per_split, float* partials
   auto& sm = *reinterpret_cast<AttnSmem<DH>*>(smem_raw);
   constexpr int NT = DH / 8;       // n-tiles of the output
 
+  grid_dep_wait();                 // Q, the index row and K/V may come from the kernels just before
+  grid_dep_trigger();
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int row = blockIdx.x;      // b * T + t
   const int split = blockIdx.y;
@@ -305,6 +307,8 @@ constexpr int MAX_SPLITS = (kMaxK + KC - 1) / KC;
 
 template <int DH>
 __global__ void attn_combine_kernel(const float* partials, int nsplit, int Hq, void* O) {
+  grid_dep_wait();
+  grid_dep_trigger();
   const int row = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
   const size_t stride = Partial::floats(DH);
   const float* base = partials + (size_t)row * nsplit * stride;
@@ -363,11 +367,10 @@ cudaError_t launch_dh(const AttnArgs& a, void* ws, size_t ws_bytes, cudaStream_t
                                        (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(rows, nsplit);
-  sparse_attn_kernel<DH><<<grid, ATHREADS, smem, st>>>(a, nsplit, cps, reinterpret_cast<float*>(ws));
-  e = cudaGetLastError();
+  e = launch_pdl(sparse_attn_kernel<DH>, grid, dim3(ATHREADS), smem, st, a, nsplit, cps, reinterpret_cast<float*>(ws));
   if (e != cudaSuccess || nsplit == 1) return e;
-  attn_combine_kernel<DH><<<dim3(rows, a.Hq), DH, 0, st>>>(reinterpret_cast<const float*>(ws), nsplit, a.Hq, a.O);
-  return cudaGetLastError();
+  return launch_pdl(attn_combine_kernel<DH>, dim3(rows, a.Hq), dim3(DH), 0, st, reinterpret_cast<const float*>(ws),
+                    nsplit, a.Hq, a.O);
 }
 
 }  // namespace
