@@ -5,10 +5,11 @@
 // to O(Lk) (notes page "NLP--IndexCache", section "背景 & 问题提出").  All
 // query heads read the one shared K/V head.
 //
-// One CTA per (query row, split).  The CTA walks its share of the index row
-// in chunks of KC positions, gathers those K and V rows into shared memory
-// through registers (double buffered: the next chunk's loads are in flight
-// during the current chunk's math), and runs a
+// One CTA per (query row, split).  The CTA loads its share of the index row
+// into shared memory once, walks it in chunks of KC positions, gathers those
+// K and V rows into shared memory through registers (double buffered: the
+// next chunk's loads are in flight during the current chunk's math, and
+// depend on no global load of their own index), and runs a
 // flash-style online softmax on the tensor cores with the heads on the MMA
 // M axis.  Four warps: two head tiles of 16 x two halves of every chunk; the
 // halves are merged at the end.  With one split the CTA writes bf16 O;
@@ -34,6 +35,7 @@ struct AttnSmem {
   __nv_bfloat16 k[2][KC][P];
   __nv_bfloat16 v[2][KC][P];
   int idx[2][KC];
+  int32_t sidx[kMaxK];         // this split's index positions, loaded once
   float m_x[HQMAX];            // merge buffers for the second key half
   float l_x[HQMAX];
   float o_x[HQMAX][DH + 4];
@@ -56,8 +58,9 @@ struct ChunkRegs {
   int s[N];                                         // source row of each piece (-1: empty slot)
 };
 
+// sidx: the split's index positions in shared memory, from position jb on.
 template <int DH>
-__device__ __forceinline__ void gather_load(ChunkRegs<DH>& g, const int32_t* irow, int j0, int k,
+__device__ __forceinline__ void gather_load(ChunkRegs<DH>& g, const int32_t* sidx, int jb, int j0, int k,
                                             const __nv_bfloat16* Kb, const __nv_bfloat16* Vb, int S, int tid) {
   constexpr int CH = ChunkRegs<DH>::CH;
 #pragma unroll
@@ -65,7 +68,7 @@ __device__ __forceinline__ void gather_load(ChunkRegs<DH>& g, const int32_t* iro
     const int i = tid + ATHREADS * u;
     const int r = i / CH, c = i % CH;
     const int j = j0 + r;
-    const int src = j < k ? __ldg(irow + j) : -1;
+    const int src = j < k ? sidx[j - jb] : -1;
     const bool ok = src >= 0 && src < S;   // an index outside [0, S) is an empty slot: never read
     g.s[u] = ok ? src : -1;
     g.k[u] = ok ? __ldcg(reinterpret_cast<const uint4*>(Kb + (size_t)src * DH) + c) : make_uint4(0u, 0u, 0u, 0u);
@@ -120,9 +123,13 @@ sparse_attn_kernel(AttnArgs a, int nsplit, int chunks_per_split, float* partials
   const int c_begin = split * chunks_per_split;
   const int c_end = min(n_chunks_total, c_begin + chunks_per_split);
 
+  // the split's index positions, in one round trip
+  const int jb = c_begin * KC, je = min(a.k, c_end * KC);
+  for (int j = jb + tid; j < je; j += ATHREADS) sm.sidx[j - jb] = __ldg(irow + j);
+  __syncthreads();
   ChunkRegs<DH> gr;
   if (c_begin < c_end) {
-    gather_load<DH>(gr, irow, c_begin * KC, a.k, Kb, Vb, a.S, tid);
+    gather_load<DH>(gr, sm.sidx, jb, c_begin * KC, a.k, Kb, Vb, a.S, tid);
     gather_store<DH>(sm, 0, gr, tid);
   }
   cp_async_wait<0>();
@@ -149,7 +156,7 @@ sparse_attn_kernel(AttnArgs a, int nsplit, int chunks_per_split, float* partials
   for (int c = c_begin; c < c_end; ++c) {
     const int buf = (c - c_begin) & 1;
     // the next chunk's loads are in flight while this one is computed
-    if (c + 1 < c_end) gather_load<DH>(gr, irow, (c + 1) * KC, a.k, Kb, Vb, a.S, tid);
+    if (c + 1 < c_end) gather_load<DH>(gr, sm.sidx, jb, (c + 1) * KC, a.k, Kb, Vb, a.S, tid);
     if (active) {
       // scores for this warp's 32 keys of the chunk: 4 n-tiles of 8 keys
       float s[4][4];
