@@ -595,8 +595,12 @@ select_finish_kernel(const float* scores, size_t pitch, const int* hist, const i
   __syncthreads();
   if (ncand > k) {
     uint32_t thr;
+    // the candidates above the threshold bin (its histogram count tells how
+    // many) are all kept; only the bin's own keys are cut
     const uint32_t lo_key = static_cast<uint32_t>(sm.bsel) << (32 - kDecHistBits);
-    cut_list<STHREADS, FSEG>(sm.key, sm.pos, ncand, k, k, lo_key, 0xFFFFFFFFu, &sm.scr, tid, BlockSync(), &thr);
+    const uint32_t hi_key = lo_key | ((1u << (32 - kDecHistBits)) - 1u);
+    const int above = ncand - hist[static_cast<size_t>(row) * HBINS + sm.bsel];
+    cut_list<STHREADS, FSEG>(sm.key, sm.pos, ncand, k, k, lo_key, hi_key, &sm.scr, tid, BlockSync(), &thr, above);
   }
   for (int j = tid; j < k; j += STHREADS) out[j] = sm.pos[j];
 }

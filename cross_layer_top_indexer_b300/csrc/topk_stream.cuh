@@ -7,9 +7,9 @@
 // order, "lower position" is "earlier in the list".
 //
 // cut_list keeps every candidate whose key is at least a threshold thr chosen
-// with a most-significant-digit histogram (8-bit digits below the bits that
-// the caller's bounds [lo, hi] share), such that at least k candidates are
-// kept.  It stops refining as soon as the kept count is at most `limit`;
+// with histograms of 256 equal-width bins over the key range still open
+// (starting from the caller's bounds [lo, hi]), such that at least k
+// candidates are kept.  It stops refining as soon as the kept count is at most `limit`;
 // with limit == k it is an exact top-k (remaining ties at thr are broken by
 // list order).  Either way, a later candidate whose key is <= thr is beaten
 // by k kept candidates, so thr is a valid insertion threshold afterwards.
@@ -79,26 +79,28 @@ __device__ int compact_keys(uint32_t* key, int* pos, int n, uint32_t thr, int eq
   return written;
 }
 
-// See the file comment.  n > k >= 1, n <= NTHREADS * SEG, lo <= key[i] <= hi
-// for every i.  Returns the kept count; *thr_out = thr.
+// See the file comment.  n > k >= 1, n <= NTHREADS * SEG.  Every entry has
+// lo <= key <= hi except exactly above0 (< k) entries with key > hi, which
+// are all kept.  Returns the kept count; *thr_out = thr.
 template <int NTHREADS, int SEG, class Sync>
 __device__ int cut_list(uint32_t* key, int* pos, int n, int k, int limit, uint32_t lo, uint32_t hi,
-                        SelectScratch* scr, int tid, Sync sync, uint32_t* thr_out) {
+                        SelectScratch* scr, int tid, Sync sync, uint32_t* thr_out, int above0 = 0) {
   const int lane = tid & 31, wid = tid >> 5;
-  int kb = lo == hi ? 32 : __clz(lo ^ hi);     // leading bits shared by every key
-  uint32_t msk = top_mask(kb), pre = hi & msk;
-  int need = k;        // still to take from the entries matching the prefix
-  int above = 0;       // entries strictly above the prefix (all kept)
-  int match = n;       // entries matching the prefix
-  while (kb < 32 && above + match > limit && match != need) {
-    const int w = min(8, 32 - kb);
-    const int shift = 32 - kb - w;
-    const uint32_t dmask = (1u << w) - 1u;
+  uint32_t rlo = lo, rhi = hi;   // the entries still to decide have rlo <= key <= rhi
+  int need = k - above0;         // still to take from them
+  int above = above0;            // entries above the range (all kept)
+  int match = n - above0;        // entries in the range
+  while (rlo < rhi && above + match > limit && match != need) {
+    // up to 256 bins of 2^shift keys each, from rlo: the bins follow the
+    // range, not the bit boundaries of the keys, so that keys crowded just
+    // above the threshold still spread over many bins
+    const uint32_t span = rhi - rlo;
+    const int shift = max(0, 24 - __clz(span));   // span >> shift <= 255
     for (int i = tid; i < 256; i += NTHREADS) scr->hist[i] = 0;
     sync();
     for (int i = tid; i < n; i += NTHREADS) {
       const uint32_t h = key[i];
-      if ((h & msk) == pre) atomicAdd(&scr->hist[(h >> shift) & dmask], 1);
+      if (h >= rlo && h <= rhi) atomicAdd(&scr->hist[(h - rlo) >> shift], 1);
     }
     sync();
     if (wid == 0) {
@@ -133,17 +135,18 @@ __device__ int cut_list(uint32_t* key, int* pos, int n, int k, int limit, uint32
     match = scr->sel_done;
     above += need - nneed;
     need = nneed;
-    pre |= dsel << shift;
-    msk |= dmask << shift;
-    kb += w;
+    const uint32_t blo = rlo + (dsel << shift);
+    const uint32_t width = (1u << shift) - 1u;   // the chosen bin is [blo, blo + width] (shift <= 24)
+    rhi = (rhi - blo <= width) ? rhi : blo + width;
+    rlo = blo;
     sync();
   }
-  // kept: everything above the prefix, then from the prefix's entries either
-  // all of them (a key >= pre) or, when the keys are fully resolved (all equal
-  // to pre), the first `need` in list order
-  const int eq_keep = (kb >= 32 && above + match > limit) ? need : n;
-  *thr_out = pre;
-  return compact_keys<NTHREADS, SEG>(key, pos, n, pre, eq_keep, scr, tid, sync);
+  // kept: everything above the range, then from the range's entries either
+  // all of them (a key >= rlo) or, when the range is one value, the first
+  // `need` in list order
+  const int eq_keep = (rlo == rhi && above + match > limit) ? need : n;
+  *thr_out = rlo;
+  return compact_keys<NTHREADS, SEG>(key, pos, n, rlo, eq_keep, scr, tid, sync);
 }
 
 }  // namespace ic
