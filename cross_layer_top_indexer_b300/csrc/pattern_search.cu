@@ -35,7 +35,7 @@ extern "C" __attribute__((visibility("default"))) ic_status ic_greedy_full_layer
   std::vector<int> remaining;
   for (int l = 1; l < n_layers; ++l) remaining.push_back(l);
   long long forwards = 0;
-  for (int round = 0; round < removals; ++round) {
+  for (int step = 0; step < removals; ++step) {
     double best_loss = 0.0;
     int best_at = -1;   // position in `remaining`
     for (size_t i = 0; i < remaining.size(); ++i) {
@@ -47,8 +47,9 @@ extern "C" __attribute__((visibility("default"))) ic_status ic_greedy_full_layer
       if (isnan(loss)) {
         memcpy(pattern_out, roles.c_str(), roles.size() + 1);
         char msg[160];
-        snprintf(msg, sizeof(msg), "the loss callback returned NaN for a trial that makes layer %d Shared (round %d)",
-                 remaining[i], round);
+        snprintf(msg, sizeof(msg),
+                 "the loss callback returned NaN for a trial that makes layer %d Shared (removal step %d)",
+                 remaining[i], step);
         return ic::report_error(IC_ERR_ARG, msg);
       }
       // `remaining` is ascending, so a strict < keeps the lower layer on a tie

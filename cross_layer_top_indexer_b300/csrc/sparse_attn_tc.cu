@@ -27,9 +27,9 @@
 //              also loads Q (TMA tile) and the index row (bulk copy) two
 //              rows ahead into a double buffer.
 //   warp 8     MMA issuer of QK^T, over the CTA's tiles in one flat sequence
-//   warp 13    MMA issuer of PV (tile g after its P is written); two issuing
-//              threads, because the issue of a tcgen05.mma holds its thread
-//              about as long as one of these N = 32 MMAs runs
+//   warp 13    MMA issuer of PV (tile g after its P is written); QK^T and PV
+//              have an issuing warp each, because the issue of a tcgen05.mma
+//              holds its thread about as long as one of these N = 32 MMAs runs
 //   warps 9-12 producers: the K rows and the V rows of every tile, gathered
 //              with 16-byte asynchronous copies into a ring of 32 KB slots
 //              (order K0 V0 K1 V1 ...) in the 128-byte-swizzled operand layout.
@@ -61,7 +61,8 @@
 // tile) is the exact tile maximum reduced across the 128 key lanes, m_h
 // moved, and the group's O columns in TMEM rescaled (after the previous PV
 // finished).  The sum l_h is kept per thread (one partial per key lane) and
-// reduced across the lanes once per row.
+// reduced across the lanes once per row; the row's output (O / l_h, bf16) is
+// written at the next row's first tile, from the other O buffer.
 //
 // Every wait is bounded; a wait that gives up sets the CTA's abort flag and
 // the device status word, every role winds down, in-flight MMAs and copies
