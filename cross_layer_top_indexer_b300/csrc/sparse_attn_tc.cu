@@ -101,6 +101,10 @@ constexpr int PROD_ROWS = KT * 16 / PROD_THREADS;   // rows of a slot each produ
 constexpr int PV_WARP = PROD_WARP0 + PROD_WARPS;   // 11
 constexpr int NTHREADS = (PV_WARP + 1) * 32;
 constexpr uint32_t TMEM_COLS = 128;          // S: 2 x 32 columns, O: 2 x 32 columns
+// Waiting threads stay suspended in try_wait for up to this long instead of
+// polling: 3.34 against 3.37 ms per layer at L = 32768 (fewer issue slots
+// taken from the softmax warps by polling producers and MMA issuers).
+constexpr uint32_t kWaitHintNs = 20000;
 constexpr float kTau = 8.0f;
 constexpr float kMInit = -1.0e30f;           // reference max before any valid key (finite: no inf - inf)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -222,9 +226,9 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         const int pb = gp & 1;
         const uint32_t itv = 2 * gp + 1;
         const int slot = static_cast<int>(itv % NSLOT);
-        if (j == 0 && !tc::mbar_wait(&sm.oempty[ob], ((n >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
-        if (!tc::mbar_wait(&sm.full[slot], (itv / NSLOT) & 1, &sm.abort)) { ok = false; break; }
-        if (!tc::mbar_wait(&sm.pfull[pb], (gp >> 1) & 1, &sm.abort)) { ok = false; break; }
+        if (j == 0 && !tc::mbar_wait<kWaitHintNs>(&sm.oempty[ob], ((n >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
+        if (!tc::mbar_wait<kWaitHintNs>(&sm.full[slot], (itv / NSLOT) & 1, &sm.abort)) { ok = false; break; }
+        if (!tc::mbar_wait<kWaitHintNs>(&sm.pfull[pb], (gp >> 1) & 1, &sm.abort)) { ok = false; break; }
         tc::tc_fence_after();
         tc::fence_proxy_async_smem();   // the gathered rows (generic-proxy copies) before the MMA reads them
         const uint32_t vb = tc::smem_u32(sm.ring[slot]);
@@ -240,7 +244,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       if (!ok) set_abort(sm, status);
       // every MMA issued so far is complete before tensor memory is released
       tc::mma_commit(&sm.drain);
-      if (!tc::mbar_wait(&sm.drain, 0, nullptr, 4000000000ull)) set_abort(sm, status);
+      if (!tc::mbar_wait<kWaitHintNs>(&sm.drain, 0, nullptr, 4000000000ull)) set_abort(sm, status);
     }
     __syncwarp();
   } else if (warp >= PROD_WARP0) {
@@ -258,7 +262,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       const int row = static_cast<int>(blockIdx.x) + n * static_cast<int>(gridDim.x);
       const int qb = n & 1;
       // a wait that gave up in any lane ends the whole warp's loop
-      if (!__all_sync(0xffffffffu, tc::mbar_wait(&sm.qfull[qb], (n >> 1) & 1, &sm.abort))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, tc::mbar_wait<kWaitHintNs>(&sm.qfull[qb], (n >> 1) & 1, &sm.abort))) { ok = false; break; }
       const size_t base_row = static_cast<size_t>(row / a.T) * a.S_cap;
       for (int j = 0; ok && j < nt; ++j) {
         int src[PROD_ROWS];
@@ -273,7 +277,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 #pragma unroll 1
         for (int kv = 0; kv < 2; ++kv, ++it) {
           const int slot = static_cast<int>(it % NSLOT);
-          const bool w_ok = tc::mbar_wait(&sm.empty[slot], ((it / NSLOT) & 1) ^ 1, &sm.abort);
+          const bool w_ok = tc::mbar_wait<kWaitHintNs>(&sm.empty[slot], ((it / NSLOT) & 1) ^ 1, &sm.abort);
           if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
           const __nv_bfloat16* base = (kv ? Vg : Kg) + base_row * DH;
           uint8_t* dst = sm.ring[slot] + half * HALF_BYTES;
@@ -300,9 +304,9 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         const int sb = g & 1;
         const uint32_t itk = 2 * g;
         const int slot = static_cast<int>(itk % NSLOT);
-        if (j == 0 && !tc::mbar_wait(&sm.qfull[qb], (n >> 1) & 1, &sm.abort)) { ok = false; break; }
-        if (!tc::mbar_wait(&sm.sempty[sb], ((g >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
-        if (!tc::mbar_wait(&sm.full[slot], (itk / NSLOT) & 1, &sm.abort)) { ok = false; break; }
+        if (j == 0 && !tc::mbar_wait<kWaitHintNs>(&sm.qfull[qb], (n >> 1) & 1, &sm.abort)) { ok = false; break; }
+        if (!tc::mbar_wait<kWaitHintNs>(&sm.sempty[sb], ((g >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
+        if (!tc::mbar_wait<kWaitHintNs>(&sm.full[slot], (itk / NSLOT) & 1, &sm.abort)) { ok = false; break; }
         tc::tc_fence_after();
         tc::fence_proxy_async_smem();
         const uint32_t kb = tc::smem_u32(sm.ring[slot]);
@@ -319,7 +323,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       if (!ok) set_abort(sm, status);
       // every MMA issued so far is complete before tensor memory is released
       tc::mma_commit(&sm.drain);
-      if (!tc::mbar_wait(&sm.drain, 0, nullptr, 4000000000ull)) set_abort(sm, status);
+      if (!tc::mbar_wait<kWaitHintNs>(&sm.drain, 0, nullptr, 4000000000ull)) set_abort(sm, status);
     }
     __syncwarp();
   } else {
@@ -343,7 +347,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     // the softmax never waits for the PV pipeline to drain at a row boundary.
     auto finish_row = [&](int m) -> bool {
       const int mb = m & 1;
-      const bool w_ok = tc::mbar_wait(&sm.ofull[mb], (m >> 1) & 1, &sm.abort);
+      const bool w_ok = tc::mbar_wait<kWaitHintNs>(&sm.ofull[mb], (m >> 1) & 1, &sm.abort);
       if (tc::named_sync_or(bar_id, GROUP_THREADS, !w_ok || sm.abort)) return false;
       tc::tc_fence_after();
       uint32_t o[HG];
@@ -360,7 +364,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       const int mrow = static_cast<int>(blockIdx.x) + m * static_cast<int>(gridDim.x);
       if (tid == 0 && m + 2 < n_rows) {
         // load row m + 2 into the buffer
-        if (tc::mbar_wait(&sm.rowfree[mb], (m >> 1) & 1, &sm.abort)) {
+        if (tc::mbar_wait<kWaitHintNs>(&sm.rowfree[mb], (m >> 1) & 1, &sm.abort)) {
           load_row_inputs(sm, &tm_q, a, mrow + 2 * static_cast<int>(gridDim.x), mb);
           rows_loaded = m + 3;
         }
@@ -375,7 +379,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     bool ok = true;
     for (int n = 0; ok && n < n_rows; ++n) {
       const int qb = n & 1;
-      if (!tc::mbar_wait(&sm.qfull[qb], (n >> 1) & 1, &sm.abort)) ok = false;
+      if (!tc::mbar_wait<kWaitHintNs>(&sm.qfull[qb], (n >> 1) & 1, &sm.abort)) ok = false;
       if (tc::named_sync_or(bar_id, GROUP_THREADS, !ok || sm.abort)) { ok = false; break; }
       float lp[HG], mr[HG];
 #pragma unroll
@@ -385,8 +389,8 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         const int pb = g & 1;
         // S(g) ready and the P buffer free (PV(g-2) done); a wait that gave up
         // is agreed on at the group's next barrier
-        bool w_ok = tc::mbar_wait(&sm.sfull[sb], (g >> 1) & 1, &sm.abort);
-        w_ok = w_ok && tc::mbar_wait(&sm.pempty[pb], ((g >> 1) & 1) ^ 1, &sm.abort);
+        bool w_ok = tc::mbar_wait<kWaitHintNs>(&sm.sfull[sb], (g >> 1) & 1, &sm.abort);
+        w_ok = w_ok && tc::mbar_wait<kWaitHintNs>(&sm.pempty[pb], ((g >> 1) & 1) ^ 1, &sm.abort);
         tc::tc_fence_after();
         uint32_t r[HG];
         tc::tmem_ld_x16(tS + sb * HQ + h0 + lane_field, r);
@@ -438,7 +442,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
           if (j > 0) {
             // this group's O columns hold tiles 0 .. j-1 once PV(g-1) is done: scale them in place
             const uint32_t gp = g - 1;
-            w_ok = tc::mbar_wait(&sm.pempty[gp & 1], (gp >> 1) & 1, &sm.abort);
+            w_ok = tc::mbar_wait<kWaitHintNs>(&sm.pempty[gp & 1], (gp >> 1) & 1, &sm.abort);
             if (tc::named_sync_or(bar_id, GROUP_THREADS, !w_ok || sm.abort)) { ok = false; break; }
             tc::tc_fence_after();
             uint32_t o[HG];
@@ -493,7 +497,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     // buffer was reused)
     if (tid == 0) {
       for (int r = rows_loaded > 2 ? rows_loaded - 2 : 0; r < rows_loaded; ++r)
-        tc::mbar_wait(&sm.qfull[r & 1], (r >> 1) & 1, nullptr);
+        tc::mbar_wait<kWaitHintNs>(&sm.qfull[r & 1], (r >> 1) & 1, nullptr);
     }
   }
 

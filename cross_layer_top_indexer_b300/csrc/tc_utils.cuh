@@ -38,15 +38,28 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// kHintNs > 0: the thread may stay suspended until the phase completes or
+// that many nanoseconds pass (fewer polls by threads that wait long).
+template <uint32_t kHintNs = 0>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
+  if constexpr (kHintNs == 0) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "n"(kHintNs)
+        : "memory");
+  }
   return ok != 0;
 }
 
@@ -71,13 +84,14 @@ constexpr uint64_t kShortWaitNs = 100000ull;
 // Wait for the phase with the given parity to complete.  Gives up after
 // `limit_ns` of wall time, or as soon as *abort is set by another thread
 // (abort may be null); returns false then and the caller winds down.
+template <uint32_t kHintNs = 0>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
                                           uint64_t limit_ns = 2000000000ull) {
   const bool short_limit = limit_ns < kShortWaitNs;
-  if (short_limit ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  if (short_limit ? mbar_test_wait(bar, parity) : mbar_try_wait<kHintNs>(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (short_limit ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (short_limit ? mbar_test_wait(bar, parity) : mbar_try_wait<kHintNs>(bar, parity)) return true;
     if (short_limit || (i & 63) == 0) {
       if (abort != nullptr && *abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) return false;
