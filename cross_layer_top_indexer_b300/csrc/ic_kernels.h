@@ -69,8 +69,13 @@ cudaError_t launch_indexer_decode_tc(const IndexerArgs& a, float* scores, size_t
 size_t attn_ws_bytes(int B, int T, int Hq, int Dh, int k);
 cudaError_t launch_sparse_attn(const AttnArgs& a, void* ws, size_t ws_bytes, int* dev_status, cudaStream_t st);
 // Tensor-core (tcgen05 + TMA gather) kernel for Hq = 32, Dh = 128 and many rows:
-bool sparse_attn_tc_supported(const AttnArgs& a);
-cudaError_t launch_sparse_attn_tc(const AttnArgs& a, int* dev_status, cudaStream_t st);
+// The tcgen05 attention: 0 when it does not take these shapes, 1 for whole
+// rows per CTA, n > 1 when each row is shared among n CTAs (few rows, e.g.
+// decode), which then write per-share partials (max, sum, unnormalised O;
+// the split kernel's layout) for the combine kernel.
+constexpr int kTcTargetCtas = 148;
+int sparse_attn_tc_splits(const AttnArgs& a);
+cudaError_t launch_sparse_attn_tc(const AttnArgs& a, int nsplit, float* partials, int* dev_status, cudaStream_t st);
 
 // Per-row overlap |I_a ∩ I_b| / k of two index tensors [R, k] (count optional).
 cudaError_t launch_overlap(int R, int k, const int32_t* ia, const int32_t* ib, float* ratio, int32_t* count,

@@ -26,6 +26,7 @@ namespace {
 constexpr int KC = 64;          // index positions per chunk
 constexpr int ATHREADS = 128;   // 4 warps
 constexpr int HQMAX = 32;
+constexpr int DHMAX = 128;      // the tcgen05 kernel's head dim (its partials use this layout)
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int DH>
@@ -388,12 +389,31 @@ size_t attn_ws_bytes(int B, int T, int Hq, int Dh, int k) {
   int nsplit = pick_splits(rows, k);
   const int cps = (n_chunks + nsplit - 1) / nsplit;
   nsplit = (n_chunks + cps - 1) / cps;
-  (void)Hq;
-  return nsplit > 1 ? (size_t)rows * nsplit * Partial::floats(Dh) * sizeof(float) : 0;
+  // the tcgen05 kernel's shares, when it takes the shapes (the key-cache
+  // size does not change the count, so the workspace covers either path)
+  AttnArgs t{};
+  t.B = B;
+  t.T = T;
+  t.Hq = Hq;
+  t.Dh = Dh;
+  t.k = k;
+  const int tsplit = sparse_attn_tc_splits(t);
+  const int most = tsplit > nsplit ? tsplit : nsplit;
+  return most > 1 ? (size_t)rows * most * Partial::floats(Dh) * sizeof(float) : 0;
 }
 
 cudaError_t launch_sparse_attn(const AttnArgs& a, void* ws, size_t ws_bytes, int* dev_status, cudaStream_t st) {
-  if (sparse_attn_tc_supported(a)) return launch_sparse_attn_tc(a, dev_status, st);
+  const int tsplit = sparse_attn_tc_splits(a);
+  if (tsplit == 1) return launch_sparse_attn_tc(a, 1, nullptr, dev_status, st);
+  if (tsplit > 1) {
+    // each row shared among tsplit CTAs of the tcgen05 kernel, then merged
+    const int rows = a.B * a.T;
+    if ((size_t)rows * tsplit * Partial::floats(DHMAX) * sizeof(float) > ws_bytes) return cudaErrorInvalidValue;
+    cudaError_t e = launch_sparse_attn_tc(a, tsplit, reinterpret_cast<float*>(ws), dev_status, st);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(attn_combine_kernel<DHMAX>, dim3(rows, a.Hq), dim3(DHMAX), 0, st,
+                      reinterpret_cast<const float*>(ws), tsplit, a.Hq, a.O);
+  }
   switch (a.Dh) {
     case 64: return launch_dh<64>(a, ws, ws_bytes, st);
     case 128: return launch_dh<128>(a, ws, ws_bytes, st);

@@ -120,6 +120,8 @@ struct __align__(1024) AttnTcSmem {
   float m_ref[HQ];
   float alpha[HQ];
   float inv_l[2][HQ];                        // per O buffer
+  float m_fin[2][HQ];                        // per O buffer: the reference max at the item's end (log2 units)
+  float l_fin[2][HQ];                        //   and the sum of its p
   uint64_t full[NSLOT], empty[NSLOT];
   uint64_t qfull[2];
   uint64_t sfull[2], sempty[2];
@@ -165,9 +167,13 @@ __device__ __forceinline__ void load_row_inputs(AttnTcSmem& sm, const CUtensorMa
   tc::bulk_g2s(sm.idx[qb], a.idx + static_cast<size_t>(row) * a.k, a.k * 4, &sm.qfull[qb]);
 }
 
+// kSplit: each row shared among nsplit CTAs (partials out); otherwise whole
+// rows (bf16 O out), with none of the share arithmetic in the loops.
+template <bool kSplit>
 __global__ void __launch_bounds__(NTHREADS, 1)
 sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, AttnArgs a, int* status) {
+                      const __grid_constant__ CUtensorMap tm_v, AttnArgs a, int nsplit, float* partials,
+                      int* status) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   AttnTcSmem& sm = *reinterpret_cast<AttnTcSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -176,11 +182,23 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   const int rows = a.B * a.T;
   const int k = a.k;
   const int nt = (k + KT - 1) / KT;
-  // rows of this CTA: blockIdx.x, blockIdx.x + gridDim.x, ...
-  const int n_rows = rows > static_cast<int>(blockIdx.x)
-                         ? (rows - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
+  // Work items: item i is tiles [j0, j0 + jn) of query row i / nsplit (whole
+  // rows when nsplit == 1; every item has at least one tile).  This CTA
+  // takes items blockIdx.x, blockIdx.x + gridDim.x, ...; n_rows counts them.
+  if constexpr (!kSplit) nsplit = 1;
+  const int tps = (nt + nsplit - 1) / nsplit;
+  const int n_items = rows * nsplit;
+  const int n_rows = n_items > static_cast<int>(blockIdx.x)
+                         ? (n_items - 1 - static_cast<int>(blockIdx.x)) / static_cast<int>(gridDim.x) + 1
                          : 0;
-  const uint32_t n_tiles = static_cast<uint32_t>(n_rows) * nt;
+  auto item_of = [&](int n) { return static_cast<int>(blockIdx.x) + n * static_cast<int>(gridDim.x); };
+  auto item_row = [&](int n) { return kSplit ? item_of(n) / nsplit : item_of(n); };
+  auto item_j0 = [&](int n) { return kSplit ? (item_of(n) % nsplit) * tps : 0; };
+  auto item_jn = [&](int n) {
+    if constexpr (!kSplit) return nt;
+    const int j0 = item_j0(n);
+    return min(nt, j0 + tps) - j0;
+  };
   // rows 0 .. smask are readable (smask + 1 is the largest power of two <= S)
   const int smask = static_cast<int>((0x80000000u >> __clz(static_cast<uint32_t>(a.S))) - 1u);
 
@@ -211,6 +229,10 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
+  // the set-up above may overlap the kernel before; Q, the index rows and K/V
+  // are read only once it has completed
+  grid_dep_wait();
+  grid_dep_trigger();
   const uint32_t tmem = sm.tmem_base;
   const uint32_t tS = tmem;          // columns 0..63: S buffers
   const uint32_t tO = tmem + 64;     // columns 64..127: O buffers
@@ -219,14 +241,15 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     // ================= MMA issuer: O^T += V^T P^T =================
     if (lane == 0) {
       bool ok = true;
-      for (uint32_t gp = 0; ok && gp < n_tiles; ++gp) {
-        const int n = static_cast<int>(gp / nt);
-        const int j = static_cast<int>(gp % nt);
+      uint32_t gp = 0;
+      for (int n = 0; ok && n < n_rows; ++n) {
+      const int j0 = item_j0(n), j1 = j0 + item_jn(n);
+      for (int j = j0; j < j1; ++j, ++gp) {
         const int ob = n & 1;
         const int pb = gp & 1;
         const uint32_t itv = 2 * gp + 1;
         const int slot = static_cast<int>(itv % NSLOT);
-        if (j == 0 && !tc::mbar_wait<kWaitHintNs>(&sm.oempty[ob], ((n >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
+        if (j == j0 && !tc::mbar_wait<kWaitHintNs>(&sm.oempty[ob], ((n >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
         if (!tc::mbar_wait<kWaitHintNs>(&sm.full[slot], (itv / NSLOT) & 1, &sm.abort)) { ok = false; break; }
         if (!tc::mbar_wait<kWaitHintNs>(&sm.pfull[pb], (gp >> 1) & 1, &sm.abort)) { ok = false; break; }
         tc::tc_fence_after();
@@ -236,10 +259,11 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 #pragma unroll
         for (int kk = 0; kk < KT / 16; ++kk)
           tc::mma_f16(tO + ob * HQ, tc::sdesc(vb + kk * 2048, HALF_BYTES, 1024, 2),
-                      tc::sdesc(pbase + kk * 1024, 0, 512, 4), IDESC_PV, (j > 0 || kk != 0) ? 1u : 0u);
+                      tc::sdesc(pbase + kk * 1024, 0, 512, 4), IDESC_PV, (j > j0 || kk != 0) ? 1u : 0u);
         tc::mma_commit(&sm.empty[slot]);
         tc::mma_commit(&sm.pempty[pb]);
-        if (j == nt - 1) tc::mma_commit(&sm.ofull[ob]);
+        if (j == j1 - 1) tc::mma_commit(&sm.ofull[ob]);
+      }
       }
       if (!ok) set_abort(sm, status);
       // every MMA issued so far is complete before tensor memory is released
@@ -259,12 +283,13 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     uint32_t it = 0;
     bool ok = true;
     for (int n = 0; ok && n < n_rows; ++n) {
-      const int row = static_cast<int>(blockIdx.x) + n * static_cast<int>(gridDim.x);
+      const int row = item_row(n);
+      const int j0 = item_j0(n), j1 = j0 + item_jn(n);
       const int qb = n & 1;
       // a wait that gave up in any lane ends the whole warp's loop
       if (!__all_sync(0xffffffffu, tc::mbar_wait<kWaitHintNs>(&sm.qfull[qb], (n >> 1) & 1, &sm.abort))) { ok = false; break; }
       const size_t base_row = static_cast<size_t>(row / a.T) * a.S_cap;
-      for (int j = 0; ok && j < nt; ++j) {
+      for (int j = j0; ok && j < j1; ++j) {
         int src[PROD_ROWS];
         const int32_t* irow = sm.idx[qb] + j * KT;
         const int lim = k - j * KT;                  // positions past k are empty slots
@@ -297,14 +322,15 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     // ================= MMA issuer: S^T = K Q^T =================
     if (lane == 0) {
       bool ok = true;
-      for (uint32_t g = 0; ok && g < n_tiles; ++g) {
-        const int n = static_cast<int>(g / nt);
-        const int j = static_cast<int>(g % nt);
+      uint32_t g = 0;
+      for (int n = 0; ok && n < n_rows; ++n) {
+      const int j0 = item_j0(n), j1 = j0 + item_jn(n);
+      for (int j = j0; j < j1; ++j, ++g) {
         const int qb = n & 1;
         const int sb = g & 1;
         const uint32_t itk = 2 * g;
         const int slot = static_cast<int>(itk % NSLOT);
-        if (j == 0 && !tc::mbar_wait<kWaitHintNs>(&sm.qfull[qb], (n >> 1) & 1, &sm.abort)) { ok = false; break; }
+        if (j == j0 && !tc::mbar_wait<kWaitHintNs>(&sm.qfull[qb], (n >> 1) & 1, &sm.abort)) { ok = false; break; }
         if (!tc::mbar_wait<kWaitHintNs>(&sm.sempty[sb], ((g >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
         if (!tc::mbar_wait<kWaitHintNs>(&sm.full[slot], (itk / NSLOT) & 1, &sm.abort)) { ok = false; break; }
         tc::tc_fence_after();
@@ -319,6 +345,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         }
         tc::mma_commit(&sm.empty[slot]);
         tc::mma_commit(&sm.sfull[sb]);
+      }
       }
       if (!ok) set_abort(sm, status);
       // every MMA issued so far is complete before tensor memory is released
@@ -338,8 +365,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     int rows_loaded = 0;                           // thread 0: rows whose inputs were requested
     if (tid == 0) {
       tc::tma_prefetch_map(&tm_q);
-      for (int n = 0; n < 2 && n < n_rows; ++n)
-        load_row_inputs(sm, &tm_q, a, static_cast<int>(blockIdx.x) + n * static_cast<int>(gridDim.x), n);
+      for (int n = 0; n < 2 && n < n_rows; ++n) load_row_inputs(sm, &tm_q, a, item_row(n), n);
       rows_loaded = n_rows < 2 ? n_rows : 2;
     }
     // Row m's output, O / l_h as bf16, once its last PV is complete.  It runs
@@ -361,30 +387,44 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         tc::mbar_arrive(&sm.oempty[mb]);
         tc::mbar_arrive(&sm.rowfree[mb]);
       }
-      const int mrow = static_cast<int>(blockIdx.x) + m * static_cast<int>(gridDim.x);
+      const int mrow = item_row(m);
       if (tid == 0 && m + 2 < n_rows) {
         // load row m + 2 into the buffer
         if (tc::mbar_wait<kWaitHintNs>(&sm.rowfree[mb], (m >> 1) & 1, &sm.abort)) {
-          load_row_inputs(sm, &tm_q, a, mrow + 2 * static_cast<int>(gridDim.x), mb);
+          load_row_inputs(sm, &tm_q, a, item_row(m + 2), mb);
           rows_loaded = m + 3;
         }
       }
-      __nv_bfloat16* Ob = reinterpret_cast<__nv_bfloat16*>(a.O) + static_cast<size_t>(mrow) * HQ * DH +
-                          static_cast<size_t>(h0) * DH + my_lane;
+      if constexpr (!kSplit) {
+        __nv_bfloat16* Ob = reinterpret_cast<__nv_bfloat16*>(a.O) + static_cast<size_t>(mrow) * HQ * DH +
+                            static_cast<size_t>(h0) * DH + my_lane;
 #pragma unroll
-      for (int h = 0; h < HG; ++h) Ob[h * DH] = __float2bfloat16_rn(__uint_as_float(o[h]) * sm.inv_l[mb][h0 + h]);
+        for (int h = 0; h < HG; ++h) Ob[h * DH] = __float2bfloat16_rn(__uint_as_float(o[h]) * sm.inv_l[mb][h0 + h]);
+      } else {
+        // a share of a row: (reference max, sum, unnormalised O) per head,
+        // merged with the row's other shares by the combine kernel
+        float* pb = partials + static_cast<size_t>(item_of(m)) * (2 * HQ + HQ * DH);
+        if (gw == 0 && lane < HG) {
+          pb[h0 + lane] = sm.m_fin[mb][h0 + lane];
+          pb[HQ + h0 + lane] = sm.l_fin[mb][h0 + lane];
+        }
+        float* po = pb + 2 * HQ + static_cast<size_t>(h0) * DH + my_lane;
+#pragma unroll
+        for (int h = 0; h < HG; ++h) po[h * DH] = __uint_as_float(o[h]);
+      }
       return true;
     };
     uint32_t g = 0;
     bool ok = true;
     for (int n = 0; ok && n < n_rows; ++n) {
       const int qb = n & 1;
+      const int j0 = item_j0(n), j1 = j0 + item_jn(n);
       if (!tc::mbar_wait<kWaitHintNs>(&sm.qfull[qb], (n >> 1) & 1, &sm.abort)) ok = false;
       if (tc::named_sync_or(bar_id, GROUP_THREADS, !ok || sm.abort)) { ok = false; break; }
       float lp[HG], mr[HG];
 #pragma unroll
       for (int h = 0; h < HG; ++h) { lp[h] = 0.0f; mr[h] = kMInit; }
-      for (int j = 0; j < nt; ++j, ++g) {
+      for (int j = j0; j < j1; ++j, ++g) {
         const int sb = g & 1;
         const int pb = g & 1;
         // S(g) ready and the P buffer free (PV(g-2) done); a wait that gave up
@@ -412,7 +452,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
           t[h] = fmaf(__uint_as_float(r[h]), sv, ov - mr[h]);
           tmax = fmaxf(tmax, t[h]);
         }
-        const bool slow = tc::named_sync_or(bar_id, GROUP_THREADS, j == 0 || tmax > kTau || !w_ok || sm.abort);
+        const bool slow = tc::named_sync_or(bar_id, GROUP_THREADS, j == j0 || tmax > kTau || !w_ok || sm.abort);
         if (slow) {
           if (tc::named_sync_or(bar_id, GROUP_THREADS, !w_ok || sm.abort)) { ok = false; break; }
           // exact tile maximum per head of the group, across the 128 key lanes
@@ -426,7 +466,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
           if (gw == 0 && lane < HG) {
             const float* rd = &sm.red[grp * 4][0];
             const float mt = fmaxf(fmaxf(rd[lane], rd[HG + lane]), fmaxf(rd[2 * HG + lane], rd[3 * HG + lane]));
-            const float mo = j == 0 ? kMInit : sm.m_ref[h0 + lane];
+            const float mo = j == j0 ? kMInit : sm.m_ref[h0 + lane];
             const float mn = fmaxf(mo, mt);
             sm.alpha[h0 + lane] = exp2f(mo - mn);
             sm.m_ref[h0 + lane] = mn;
@@ -439,7 +479,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             mr[h] = mn;
             lp[h] *= sm.alpha[h0 + h];
           }
-          if (j > 0) {
+          if (j > j0) {
             // this group's O columns hold tiles 0 .. j-1 once PV(g-1) is done: scale them in place
             const uint32_t gp = g - 1;
             w_ok = tc::mbar_wait<kWaitHintNs>(&sm.pempty[gp & 1], (gp >> 1) & 1, &sm.abort);
@@ -478,7 +518,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         tc::tc_fence_before();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&sm.pfull[pb]);
-        if (j == 0 && n > 0 && !finish_row(n - 1)) { ok = false; break; }
+        if (j == j0 && n > 0 && !finish_row(n - 1)) { ok = false; break; }
       }
       if (!ok) break;
       // ---- row end: l_h (the output is written by finish_row) ----
@@ -488,6 +528,8 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         const float* rd = &sm.red[grp * 4][0];
         const float l = rd[lane] + rd[HG + lane] + rd[2 * HG + lane] + rd[3 * HG + lane];
         sm.inv_l[qb][h0 + lane] = l > 0.0f ? 1.0f / l : 0.0f;
+        sm.l_fin[qb][h0 + lane] = l;
+        sm.m_fin[qb][h0 + lane] = sm.m_ref[h0 + lane];
       }
     }
     if (ok && n_rows > 0 && !finish_row(n_rows - 1)) ok = false;
@@ -509,16 +551,26 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 
 }  // namespace
 
-bool sparse_attn_tc_supported(const AttnArgs& a) {
-  // k > KT: a row spans at least two tiles, so the slots a producer still
-  // holds back at a row boundary all belong to the current row
-  return a.Hq == HQ && a.Dh == DH && (a.k % 4) == 0 && a.k > KT && static_cast<long long>(a.B) * a.T >= 2 * 148 &&
-         static_cast<long long>(a.B) * a.T * HQ < (1ll << 31) && static_cast<long long>(a.B) * a.S_cap < (1ll << 31);
+int sparse_attn_tc_splits(const AttnArgs& a) {
+  const long long rows = static_cast<long long>(a.B) * a.T;
+  if (a.Hq != HQ || a.Dh != DH || (a.k % 4) != 0 || a.k <= KT || rows * HQ >= (1ll << 31) ||
+      static_cast<long long>(a.B) * a.S_cap >= (1ll << 31))
+    return 0;
+  if (rows >= 2 * kTcTargetCtas) return 1;   // whole rows, at least two per CTA
+  // few rows (decode): each row's tiles are shared among up to
+  // kTcTargetCtas / rows CTAs, at least two tiles each
+  const int nt = (a.k + KT - 1) / KT;
+  int ns = static_cast<int>(kTcTargetCtas / rows);
+  ns = ns < nt / 2 ? ns : nt / 2;
+  if (ns < 2) return 0;
+  const int tps = (nt + ns - 1) / ns;
+  return (nt + tps - 1) / tps;                 // every share non-empty
 }
 
-cudaError_t launch_sparse_attn_tc(const AttnArgs& a, int* dev_status, cudaStream_t st) {
+cudaError_t launch_sparse_attn_tc(const AttnArgs& a, int nsplit, float* partials, int* dev_status, cudaStream_t st) {
   CUtensorMap tm_q, tm_k, tm_v;
   const uint64_t rows = static_cast<uint64_t>(a.B) * a.T;
+  if (nsplit < 1 || (nsplit > 1 && partials == nullptr)) return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&tm_q, a.Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows * HQ, DH, HQ, 64))
     return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&tm_k, a.K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(a.B) * a.S_cap, DH, 1,
@@ -531,12 +583,12 @@ cudaError_t launch_sparse_attn_tc(const AttnArgs& a, int* dev_status, cudaStream
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
   const size_t smem = sizeof(AttnTcSmem) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(sparse_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  auto kern = nsplit > 1 ? sparse_attn_tc_kernel<true> : sparse_attn_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  const int grid = static_cast<int>(rows < static_cast<uint64_t>(n_sm) ? rows : n_sm);
-  sparse_attn_tc_kernel<<<grid, NTHREADS, smem, st>>>(tm_q, tm_k, tm_v, a, dev_status);
-  return cudaGetLastError();
+  const uint64_t items = rows * static_cast<uint64_t>(nsplit);
+  const int grid = static_cast<int>(items < static_cast<uint64_t>(n_sm) ? items : n_sm);
+  return launch_pdl(kern, dim3(grid), dim3(NTHREADS), smem, st, tm_q, tm_k, tm_v, a, nsplit, partials, dev_status);
 }
 
 }  // namespace ic
