@@ -19,7 +19,10 @@
 // so the softmax thread that owns key lane j holds that key's 32 head
 // scores, and the output accumulates in TMEM with d on the lanes.
 //
-// Persistent CTAs (one per SM) walk query rows row = blockIdx.x + i*gridDim.x.
+// Persistent CTAs (one per SM) walk work items item = blockIdx.x + i*gridDim.x:
+// whole query rows, or, with few rows (decode), a range of a row's tiles, in
+// which case the CTA writes the share's reference max, sum and unnormalised O
+// and a combine kernel merges the shares of a row.
 // Warp roles (14 warps):
 //   warps 0-7  softmax + epilogue in two head groups: warps 0-3 own heads
 //              0-15, warps 4-7 heads 16-31 (warp w reads TMEM lane quarter
