@@ -245,27 +245,34 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     if (lane == 0) {
       bool ok = true;
       uint32_t gp = 0;
+      // the V tile of tile g is ring item 2g + 1: its slot and phase advance
+      // by two items per tile; descriptors are built once and only their
+      // start address moves (by 16-byte units, within the 256 KB window)
+      int slot = 1;
+      uint32_t phase = 0;
+      const uint64_t dv0 = tc::sdesc(tc::smem_u32(sm.ring[0]), HALF_BYTES, 1024, 2);
+      const uint64_t dp0 = tc::sdesc(tc::smem_u32(sm.ps[0]), 0, 512, 4);
       for (int n = 0; ok && n < n_rows; ++n) {
       const int j0 = item_j0(n), j1 = j0 + item_jn(n);
       for (int j = j0; j < j1; ++j, ++gp) {
         const int ob = n & 1;
         const int pb = gp & 1;
-        const uint32_t itv = 2 * gp + 1;
-        const int slot = static_cast<int>(itv % NSLOT);
         if (j == j0 && !tc::mbar_wait<kWaitHintNs>(&sm.oempty[ob], ((n >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
-        if (!tc::mbar_wait<kWaitHintNs>(&sm.full[slot], (itv / NSLOT) & 1, &sm.abort)) { ok = false; break; }
+        if (!tc::mbar_wait<kWaitHintNs>(&sm.full[slot], phase, &sm.abort)) { ok = false; break; }
         if (!tc::mbar_wait<kWaitHintNs>(&sm.pfull[pb], (gp >> 1) & 1, &sm.abort)) { ok = false; break; }
         tc::tc_fence_after();
         tc::fence_proxy_async_smem();   // the gathered rows (generic-proxy copies) before the MMA reads them
-        const uint32_t vb = tc::smem_u32(sm.ring[slot]);
-        const uint32_t pbase = tc::smem_u32(sm.ps[pb]);
+        const uint64_t dv = dv0 + static_cast<uint64_t>(slot * (SLOT_BYTES >> 4));
+        const uint64_t dp = dp0 + static_cast<uint64_t>(pb * (P_BYTES >> 4));
 #pragma unroll
         for (int kk = 0; kk < KT / 16; ++kk)
-          tc::mma_f16(tO + ob * HQ, tc::sdesc(vb + kk * 2048, HALF_BYTES, 1024, 2),
-                      tc::sdesc(pbase + kk * 1024, 0, 512, 4), IDESC_PV, (j > j0 || kk != 0) ? 1u : 0u);
+          tc::mma_f16(tO + ob * HQ, dv + kk * (2048 >> 4), dp + kk * (1024 >> 4), IDESC_PV,
+                      (j > j0 || kk != 0) ? 1u : 0u);
         tc::mma_commit(&sm.empty[slot]);
         tc::mma_commit(&sm.pempty[pb]);
         if (j == j1 - 1) tc::mma_commit(&sm.ofull[ob]);
+        slot += 2;
+        if (slot >= NSLOT) { slot -= NSLOT; phase ^= 1u; }
       }
       }
       if (!ok) set_abort(sm, status);
@@ -283,7 +290,8 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     const int r0 = pt >> 4;                          // rows r0, r0 + RSTEP, ...
     const __nv_bfloat16* Kg = reinterpret_cast<const __nv_bfloat16*>(a.K) + c * 8;
     const __nv_bfloat16* Vg = reinterpret_cast<const __nv_bfloat16*>(a.V) + c * 8;
-    uint32_t it = 0;
+    int slot = 0;                                    // ring item: K0 V0 K1 V1 ...
+    uint32_t phase = 0;
     bool ok = true;
     for (int n = 0; ok && n < n_rows; ++n) {
       const int row = item_row(n);
@@ -303,9 +311,8 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
           src[i] = (s >= 0 && s < a.S) ? s : ((j * KT + r) & smask);   // empty slot: a spread, readable row
         }
 #pragma unroll 1
-        for (int kv = 0; kv < 2; ++kv, ++it) {
-          const int slot = static_cast<int>(it % NSLOT);
-          const bool w_ok = tc::mbar_wait<kWaitHintNs>(&sm.empty[slot], ((it / NSLOT) & 1) ^ 1, &sm.abort);
+        for (int kv = 0; kv < 2; ++kv) {
+          const bool w_ok = tc::mbar_wait<kWaitHintNs>(&sm.empty[slot], phase ^ 1u, &sm.abort);
           if (!__all_sync(0xffffffffu, w_ok)) { ok = false; break; }
           const __nv_bfloat16* base = (kv ? Vg : Kg) + base_row * DH;
           uint8_t* dst = sm.ring[slot] + half * HALF_BYTES;
@@ -315,6 +322,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
             cp_async16(dst + r * 128 + ((cc ^ (r & 7)) << 4), base + static_cast<size_t>(src[i]) * DH, true);
           }
           cp_async_arrive_noinc(&sm.full[slot]);
+          if (++slot == NSLOT) { slot = 0; phase ^= 1u; }
         }
       }
     }
@@ -326,28 +334,34 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     if (lane == 0) {
       bool ok = true;
       uint32_t g = 0;
+      // the K tile of tile g is ring item 2g (slot and phase advance by two
+      // items per tile); descriptors as in the PV issuer
+      int slot = 0;
+      uint32_t phase = 0;
+      const uint64_t dk0 = tc::sdesc_k_sw128(tc::smem_u32(sm.ring[0]));
+      const uint64_t dq0 = tc::sdesc_k_sw128(tc::smem_u32(sm.qs[0]));
       for (int n = 0; ok && n < n_rows; ++n) {
       const int j0 = item_j0(n), j1 = j0 + item_jn(n);
       for (int j = j0; j < j1; ++j, ++g) {
         const int qb = n & 1;
         const int sb = g & 1;
-        const uint32_t itk = 2 * g;
-        const int slot = static_cast<int>(itk % NSLOT);
         if (j == j0 && !tc::mbar_wait<kWaitHintNs>(&sm.qfull[qb], (n >> 1) & 1, &sm.abort)) { ok = false; break; }
         if (!tc::mbar_wait<kWaitHintNs>(&sm.sempty[sb], ((g >> 1) & 1) ^ 1, &sm.abort)) { ok = false; break; }
-        if (!tc::mbar_wait<kWaitHintNs>(&sm.full[slot], (itk / NSLOT) & 1, &sm.abort)) { ok = false; break; }
+        if (!tc::mbar_wait<kWaitHintNs>(&sm.full[slot], phase, &sm.abort)) { ok = false; break; }
         tc::tc_fence_after();
         tc::fence_proxy_async_smem();
-        const uint32_t kb = tc::smem_u32(sm.ring[slot]);
-        const uint32_t q0 = tc::smem_u32(sm.qs[qb]);
+        const uint64_t dk = dk0 + static_cast<uint64_t>(slot * (SLOT_BYTES >> 4));
+        const uint64_t dq = dq0 + static_cast<uint64_t>(qb * (Q_BYTES >> 4));
 #pragma unroll
         for (int kk = 0; kk < DH / 16; ++kk) {
           const uint32_t off = (kk >> 2) * HALF_BYTES + (kk & 3) * 32;
           const uint32_t qoff = (kk >> 2) * (Q_BYTES / 2) + (kk & 3) * 32;
-          tc::mma_f16(tS + sb * HQ, tc::sdesc_k_sw128(kb + off), tc::sdesc_k_sw128(q0 + qoff), IDESC_QK, kk != 0);
+          tc::mma_f16(tS + sb * HQ, dk + (off >> 4), dq + (qoff >> 4), IDESC_QK, kk != 0);
         }
         tc::mma_commit(&sm.empty[slot]);
         tc::mma_commit(&sm.sfull[sb]);
+        slot += 2;
+        if (slot >= NSLOT) { slot -= NSLOT; phase ^= 1u; }
       }
       }
       if (!ok) set_abort(sm, status);
