@@ -605,6 +605,18 @@ select_finish_kernel(const float* scores, size_t pitch, const int* hist, const i
   for (int j = tid; j < k; j += STHREADS) out[j] = sm.pos[j];
 }
 
+// Clears the score histograms before the scorer adds into them.  A kernel
+// (not a memset) so that the launches around it keep their programmatic
+// dependent launch edges; it waits for the kernel before it, which may
+// still read the previous call's histograms.
+__global__ void __launch_bounds__(256) zero_words_kernel(uint4* p, size_t n16) {
+  grid_dep_wait();
+  grid_dep_trigger();
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n16;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 cudaError_t launch_chunked_select(const DecWs& d, const IndexerArgs& a, cudaStream_t st) {
   const int n = a.q_pos0 + 1;                    // one row per sequence (T = 1)
   if (n > a.k) {
@@ -656,7 +668,10 @@ cudaError_t launch_indexer_decode(const IndexerArgs& a, void* ws, size_t ws_byte
     const DecWs d = carve_ws(ws, a.B * a.T, a.S, &need);
     if (ws_bytes >= need) {
       // histogram built by the scorer, then the chunked select
-      e = cudaMemsetAsync(d.hist, 0, static_cast<size_t>(a.B) * a.T * HBINS * sizeof(int), st);
+      // rows * HBINS ints: a whole number of 16-byte words (HBINS is a multiple of 4)
+      const size_t n16 = static_cast<size_t>(a.B) * a.T * HBINS / 4;
+      e = launch_pdl(zero_words_kernel, dim3(static_cast<unsigned>((n16 + 255) / 256 < 148 ? (n16 + 255) / 256 : 148)),
+                     dim3(256), 0, st, reinterpret_cast<uint4*>(d.hist), n16);
       if (e != cudaSuccess) return e;
       e = launch_indexer_decode_tc(a, scores, pitch, d.hist, dev_status, st);
       if (e != cudaSuccess) return e;
