@@ -380,6 +380,8 @@ def _attn_case(Bn, T, S, S_cap, k, mode, seed):
     (3, 1, 700, 700, 100, "spike"),           # one dominant key
     (4, 1, 2000, 2000, 1024, "growing"),      # later splits hold the larger scores
     (6, 1, 3000, 3000, 512, "masked_head"),   # an empty first chunk, empty rows, out-of-range slots
+    (3, 1, 4000, 4000, 1152, "growing"),      # 9 tiles of 128 keys shared 3 + 3 + 3 among CTAs
+    (7, 1, 2500, 2600, 644, "spike"),         # 6 tiles, the last with 4 keys, shared 2 + 2 + 2
 ])
 def test_decode_attention_split_cases(Bn, T, S, S_cap, k, mode):
     # few rows: the k positions are split across CTAs and the splits merged
