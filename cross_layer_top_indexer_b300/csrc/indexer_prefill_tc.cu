@@ -18,8 +18,9 @@
 //   warp 1     TMEM allocator + MMA issuer
 //   warps 2-17 epilogue: four warpgroups; warpgroup g owns query row g.
 //              Thread = one key (its TMEM lane); it reads the 64 head dot
-//              products of its row in two halves, forms the weighted ReLU
-//              sum in registers, and runs the streaming top-k.
+//              products of its row in quarters of 16 (each quarter's load
+//              in flight while the previous one is summed), forms the
+//              weighted ReLU sum in registers, and runs the streaming top-k.
 //
 // e4m3 keys: every e4m3 value (subnormals included) is a bf16 value, so a
 // small kernel first widens the keys the call reads into a bf16 copy in the
@@ -340,15 +341,42 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
           }
         };
         if constexpr (RPW == 1) {
-          // one half of the heads at a time (fewer live registers; the other
-          // epilogue warps of the sub-partition cover the load latency)
-          uint32_t r[32];
-          tc::tmem_ld_x32(col, r);
+          // quarters of 16 heads, each quarter's load in flight while the one
+          // before is summed (two 16-register buffers, as many live registers
+          // as one 32-column load)
+          auto acc16 = [&](const uint32_t (&r)[16], const float* wh) {
+#pragma unroll
+            for (int h = 0; h < 16; h += 4) {
+              const float4 w4 = *reinterpret_cast<const float4*>(wh + h);
+              s0 = fmaf(w4.x, fmaxf(__uint_as_float(r[h + 0]), 0.0f), s0);
+              s1 = fmaf(w4.y, fmaxf(__uint_as_float(r[h + 1]), 0.0f), s1);
+              s2 = fmaf(w4.z, fmaxf(__uint_as_float(r[h + 2]), 0.0f), s2);
+              s3 = fmaf(w4.w, fmaxf(__uint_as_float(r[h + 3]), 0.0f), s3);
+            }
+          };
+          // the values of a load are used only after its wait
+          auto fence16 = [](uint32_t (&r)[16]) {
+            asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                         "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                         "+r"(r[14]), "+r"(r[15]));
+          };
+          uint32_t ra[16], rb[16];
+          tc::tmem_ld_x16(col, ra);
           tc::tmem_wait_ld();
-          accumulate(r, wq);
-          tc::tmem_ld_x32(col + 32, r);
+          fence16(ra);
+          tc::tmem_ld_x16(col + 16, rb);
+          acc16(ra, wq);
           tc::tmem_wait_ld();
-          accumulate(r, wq + 32);
+          fence16(rb);
+          tc::tmem_ld_x16(col + 32, ra);
+          acc16(rb, wq + 16);
+          tc::tmem_wait_ld();
+          fence16(ra);
+          tc::tmem_ld_x16(col + 48, rb);
+          acc16(ra, wq + 32);
+          tc::tmem_wait_ld();
+          fence16(rb);
+          acc16(rb, wq + 48);
         } else {
           uint32_t r0[32], r1[32];
           tc::tmem_ld_x32(col, r0);
