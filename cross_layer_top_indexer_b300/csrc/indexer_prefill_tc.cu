@@ -101,7 +101,7 @@ struct __align__(1024) TcSmem {
   uint32_t tmem_base;
   int abort;
   // per tile parity, row and key quarter: insert count
-  int xc[2][QPB][4];
+  alignas(16) int xc[2][QPB][4];
   SelectScratch scr[QPB];
 };
 
@@ -408,7 +408,8 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
 #pragma unroll
       for (int qq = 0; qq < RPW; ++qq) {
         const int qi = q0 + qq;
-        int tot = sm.xc[par][qi][0] + sm.xc[par][qi][1] + sm.xc[par][qi][2] + sm.xc[par][qi][3];
+        int4 cv = *reinterpret_cast<const int4*>(&sm.xc[par][qi][0]);   // the four warps' counts, one load
+        int tot = (cv.x + cv.y) + (cv.z + cv.w);
         if (cnt[qq] + tot > CAP) {
           // the list would overflow: cut it, raise tau, recount this tile's keys
           uint32_t thr;
@@ -420,11 +421,12 @@ indexer_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid
           bal[qq] = __ballot_sync(0xffffffffu, take[qq]);
           if (lane == 0) sm.xc[par][qi][quarter] = __popc(bal[qq]);
           wsync();
-          tot = sm.xc[par][qi][0] + sm.xc[par][qi][1] + sm.xc[par][qi][2] + sm.xc[par][qi][3];
+          cv = *reinterpret_cast<const int4*>(&sm.xc[par][qi][0]);
+          tot = (cv.x + cv.y) + (cv.z + cv.w);
         }
         if (tot == 0) continue;
         int off = cnt[qq];
-        for (int x = 0; x < quarter; ++x) off += sm.xc[par][qi][x];
+        off += (quarter > 0 ? cv.x : 0) + (quarter > 1 ? cv.y : 0) + (quarter > 2 ? cv.z : 0);
         if (take[qq]) {
           const int slot = off + __popc(bal[qq] & lanes_below);
           sm.cand_k[qi][slot] = key[qq];
