@@ -148,7 +148,7 @@ def launches_per_forward(pattern, B, T, k):
 
 # names of this library's kernels (substrings of the CUDA kernel names)
 OUR_KERNELS = ("indexer_prefill_tc_kernel", "indexer_prefill_kernel", "widen_e4m3_keys_kernel",
-               "indexer_decode_tc_kernel", "decode_scores_kernel", "select_chunk_kernel", "select_finish_kernel",
+               "indexer_decode_tc_kernel", "decode_scores_kernel", "select_cluster_kernel",
                "decode_select_kernel", "sparse_attn_tc_kernel", "sparse_attn_kernel", "attn_combine_kernel",
                "decode_append_kernel", "overlap_kernel")
 

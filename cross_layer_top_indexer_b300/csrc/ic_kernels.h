@@ -48,9 +48,8 @@ bool encode_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType dtyp
 
 // Decode indexer: score rows into ws, then an exact select per row.
 // indexer_decode_ws_bytes is the least workspace the path needs (the score
-// rows); indexer_decode_ws_fast_bytes adds the histogram, chunk counts and
-// candidate buffers of the chunked select, which the path uses when the
-// workspace holds them.
+// rows); indexer_decode_ws_fast_bytes adds the score-key histogram of the
+// clustered select, which the path uses when the workspace holds it.
 size_t indexer_decode_ws_bytes(int B, int T, int S);
 size_t indexer_decode_ws_fast_bytes(int B, int T, int S);
 cudaError_t launch_indexer_decode(const IndexerArgs& a, void* ws, size_t ws_bytes, int* dev_status,

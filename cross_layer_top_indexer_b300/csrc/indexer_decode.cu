@@ -11,14 +11,19 @@
 // sequence with H = 64, d = 128; otherwise decode_scores_kernel below (one
 // CTA per (tile of keys, query row), mma.sync).
 // Select: with the tensor-core scorer and a workspace that holds the
-// histogram and candidate buffers, the chunked select (select_chunk_kernel +
-// select_finish_kernel); otherwise decode_select_kernel, one CTA per row.
+// histogram, the clustered select (select_cluster_kernel, a cluster of CTAs
+// per row); otherwise decode_select_kernel, one CTA per row.
+#include <cooperative_groups.h>
+
 #include "ic_common.cuh"
 #include "ic_kernels.h"
+#include "tc_utils.cuh"
 #include "topk_stream.cuh"
 
 namespace ic {
 namespace {
+
+namespace cg = cooperative_groups;
 
 constexpr int DKT = 256;          // keys per scoring CTA (8 warps x 32)
 constexpr int DTHREADS = 256;
@@ -423,32 +428,31 @@ cudaError_t launch_select(float* scores, size_t pitch, const IndexerArgs& a, cud
 }
 
 // ---------------------------------------------------------------------------
-// Chunked select (one query row per sequence, after the tensor-core scorer,
-// which leaves a histogram of each row's score keys by their top
+// Clustered select (one query row per sequence, after the tensor-core
+// scorer, which leaves a histogram of each row's score keys by their top
 // kDecHistBits bits).  The threshold bin is the bin of the k-th largest key;
-// the entries in and above it are the candidates.
-//   select_chunk_kernel   one CTA per (chunk of CH scores, row): writes the
-//                         positions of its candidates and their keys, in
-//                         order, to the chunk's region, and their count
-//   select_finish_kernel  one CTA per row: a warp per chunk copies the
-//                         chunk's (position, key) lists, coalesced, into
-//                         shared memory in chunk order (= position order),
-//                         then cuts them to exactly k
-// Rows with more candidates than FCAP take the general radix path.
+// the entries in and above it are the row's ncand candidates.  A cluster of
+// SCL CTAs takes one row: CTA r copies the r-th part of the score row into
+// its shared memory with bulk copies (plain loads are held back by the few
+// misses an SM keeps in flight: the row has usually left L2 by then) and
+// lists its candidates (key, position), in position order; after the
+// cluster barrier every CTA stores its list into CTA 0's, after the lists of
+// the CTAs before it, through distributed shared memory; CTA 0 then cuts the
+// threshold bin's entries to exactly k (the candidates above the bin are all
+// kept) and writes the positions, which are already ascending.  Rows with
+// more than FCAP candidates, or whose lists disagree with the histogram,
+// take the general radix path.
 // ---------------------------------------------------------------------------
 constexpr int HBINS = 1 << kDecHistBits;
-constexpr int CH = 4096;                 // scores per chunk
-constexpr int CTHREADS = 256;            // 16 scores per thread
-constexpr int FCH = 2048;                // chunks per row the finish kernel indexes (rows up to 8 Mi keys)
+constexpr int SCL = 4;                   // CTAs per row (one cluster)
+constexpr int SUNR = 17;                 // 16-byte reads per thread per pass
+constexpr int SPASS = STHREADS * 4 * SUNR;   // scores per pass: a quarter of a 131K-key row in one
+constexpr int SPIECE = 16384;            // bytes per bulk copy
 
 struct DecWs {
   float* scores;
   int* hist;    // [rows][HBINS]
-  int* cnt;     // [rows][nch]
-  int* cand;    // [rows][nch][CH]: positions
-  uint32_t* candk;   // [rows][nch][CH]: their keys
   size_t pitch;
-  int nch;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -456,19 +460,12 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 DecWs carve_ws(void* ws, int rows, int S, size_t* total) {
   DecWs d;
   d.pitch = row_pitch(S);
-  d.nch = static_cast<int>((d.pitch + CH - 1) / CH);
   unsigned char* p = static_cast<unsigned char*>(ws);
   size_t off = 0;
   d.scores = reinterpret_cast<float*>(p + off);
   off += align256(static_cast<size_t>(rows) * d.pitch * sizeof(float));
   d.hist = reinterpret_cast<int*>(p + off);
   off += align256(static_cast<size_t>(rows) * HBINS * sizeof(int));
-  d.cnt = reinterpret_cast<int*>(p + off);
-  off += align256(static_cast<size_t>(rows) * d.nch * sizeof(int));
-  d.cand = reinterpret_cast<int*>(p + off);
-  off += align256(static_cast<size_t>(rows) * d.nch * CH * sizeof(int));
-  d.candk = reinterpret_cast<uint32_t*>(p + off);
-  off += align256(static_cast<size_t>(rows) * d.nch * CH * sizeof(uint32_t));
   *total = off;
   return d;
 }
@@ -498,109 +495,139 @@ __device__ void threshold_bin(const int* h, int k, int* warp_sums, int* s_bsel, 
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(CTHREADS)
-select_chunk_kernel(const float* scores, size_t pitch, const int* hist, int* cnt, int* cand, uint32_t* candk, int nch,
-                    int n, int k) {
-  __shared__ int warp_sums[32];
-  __shared__ int s_bsel, s_ncand;
-  grid_dep_wait();                               // the scores and the histogram of the scorer just before
-  grid_dep_trigger();
-  const int row = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
-  if (n <= k) return;                            // the finish kernel writes 0 .. n-1
-  threshold_bin<CTHREADS>(hist + static_cast<size_t>(row) * HBINS, k, warp_sums, &s_bsel, &s_ncand);
-  if (s_ncand > FCAP) return;                    // the finish kernel takes the radix path
-  const uint32_t lo = static_cast<uint32_t>(s_bsel) << (32 - kDecHistBits);
-  const float* sc = scores + static_cast<size_t>(row) * pitch;
-  const int i0 = c * CH + 16 * tid;
-  float v[16];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float4 x = load_row4(sc, i0 + 4 * j, n);
-    v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
-  }
-  unsigned f = 0;
-  int cl = 0;
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    if (i0 + j < n && float_key(v[j]) >= lo) { f |= 1u << j; ++cl; }
-  int tot;
-  int off = block_exclusive_scan(cl, warp_sums, CTHREADS, tot, tid, BlockSync());
-  int* dst = cand + (static_cast<size_t>(row) * nch + c) * CH;
-  uint32_t* dstk = candk + (static_cast<size_t>(row) * nch + c) * CH;
-#pragma unroll
-  for (int j = 0; j < 16; ++j)
-    if (f & (1u << j)) {
-      dst[off] = i0 + j;
-      dstk[off] = float_key(v[j]);
-      ++off;
-    }
-  if (tid == 0) cnt[static_cast<size_t>(row) * nch + c] = tot;
-}
-
-struct FinishSmem {
+struct __align__(128) ClusterSelSmem {
+  float buf[SPASS];                      // a pass of this CTA's part of the score row
   uint32_t key[FCAP];
   int pos[FCAP];
-  int coff[FCH + 1];
   SelectScratch scr;
-  int bsel, ncand;
+  uint64_t bar;
+  int bsel, ncand, count, good;
 };
 
-__global__ void __launch_bounds__(STHREADS)
-select_finish_kernel(const float* scores, size_t pitch, const int* hist, const int* cnt, const int* cand,
-                     const uint32_t* candk, int nch, int32_t* idx, int n, int k) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  FinishSmem& sm = *reinterpret_cast<FinishSmem*>(smem_raw);
-  grid_dep_wait();                               // the chunk kernel's lists and counts
+__global__ void __cluster_dims__(SCL, 1, 1) __launch_bounds__(STHREADS)
+select_cluster_kernel(const float* scores, size_t pitch, const int* hist, int32_t* idx, int n, int k, int* status) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  ClusterSelSmem& sm = *reinterpret_cast<ClusterSelSmem*>(smem_raw);
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int row = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    tc::mbar_init(&sm.bar, 1);
+    tc::fence_mbar_init();
+  }
+  grid_dep_wait();                               // the scores and the histogram of the scorer just before
   grid_dep_trigger();
-  const int row = blockIdx.x, tid = threadIdx.x;
   const float* sc = scores + static_cast<size_t>(row) * pitch;
   int32_t* out = idx + static_cast<size_t>(row) * k;
+  // the branches below depend only on (n, k, the row's histogram): every CTA
+  // of the cluster takes the same one
   if (n <= k) {
-    for (int j = tid; j < k; j += STHREADS) out[j] = j < n ? j : -1;
+    if (rank == 0)
+      for (int j = tid; j < k; j += STHREADS) out[j] = j < n ? j : -1;
     return;
   }
-  threshold_bin<STHREADS>(hist + static_cast<size_t>(row) * HBINS, k, sm.scr.warp_sums, &sm.bsel, &sm.ncand);
+  const int* hrow = hist + static_cast<size_t>(row) * HBINS;
+  threshold_bin<STHREADS>(hrow, k, sm.scr.warp_sums, &sm.bsel, &sm.ncand);   // ends with a CTA barrier
   const int ncand = sm.ncand;
-  const int nc = (n + CH - 1) / CH;              // chunks of this row
-  if (ncand > FCAP || nc > FCH) {
-    radix_select_row(sc, n, k, out);
+  if (ncand > FCAP) {
+    if (rank == 0) radix_select_row(sc, n, k, out);
     return;
   }
-  // chunk offsets (exclusive prefix of the counts), then the candidates in order
-  const int* crow = cnt + static_cast<size_t>(row) * nch;
+  // this CTA's part of the row (a multiple of 4 scores, so copies stay 16-byte aligned)
+  const uint32_t lo = static_cast<uint32_t>(sm.bsel) << (32 - kDecHistBits);
+  const int part = ((n + SCL - 1) / SCL + 3) & ~3;
+  const int p0 = min(n, rank * part), p1 = min(n, p0 + part);
+  // Thread t lists the scores [4 SUNR t, 4 SUNR (t + 1)) of each pass, so
+  // the pass's position order is the thread order.  A thread marks its
+  // candidates in a bit mask as it reads them (independent 16-byte reads,
+  // 272 bytes apart: distinct banks within each 8-thread phase) and then
+  // visits only the marked ones, about 2 of its 68 scores on average.
   int run = 0;
-  for (int c0 = 0; c0 < nc; c0 += STHREADS) {
-    const int v = c0 + tid < nc ? crow[c0 + tid] : 0;
+  bool ok = true;
+  uint32_t phase = 0;
+  for (int base = p0; base < p1; base += SPASS, phase ^= 1u) {
+    if (tid == 0) {
+      // up to the row's pitch, which holds n rounded up to 4 scores
+      const uint32_t bytes = static_cast<uint32_t>(((min(p1 - base, SPASS) + 3) & ~3) * sizeof(float));
+      tc::fence_proxy_async_smem();              // the last pass's reads of buf come before these writes
+      tc::mbar_arrive_expect_tx(&sm.bar, bytes);
+      for (uint32_t off = 0; off < bytes; off += SPIECE)
+        tc::bulk_g2s(reinterpret_cast<char*>(sm.buf) + off, reinterpret_cast<const char*>(sc + base) + off,
+                     min(static_cast<uint32_t>(SPIECE), bytes - off), &sm.bar);
+    }
+    if (!tc::mbar_wait(&sm.bar, phase, nullptr)) {
+      ok = false;                                // a copy may still land: waited for again before the exit
+      if (status) atomicExch(status, kDevTimeout);
+    }
+    const int t0 = 4 * SUNR * tid;               // this thread's first entry of the pass
+    const int nmine = max(0, min(4 * SUNR, p1 - base - t0));
+    const float4* mine = reinterpret_cast<const float4*>(&sm.buf[t0]);
+    uint32_t m[(SUNR + 7) / 8] = {};             // bit 4 j + c: entry 4 j + c is a candidate
+#pragma unroll
+    for (int j = 0; j < SUNR; ++j) {
+      const float4 x = mine[j];
+      const uint32_t f = (float_key(x.x) >= lo ? 1u : 0u) | (float_key(x.y) >= lo ? 2u : 0u) |
+                         (float_key(x.z) >= lo ? 4u : 0u) | (float_key(x.w) >= lo ? 8u : 0u);
+      m[j >> 3] |= f << (4 * (j & 7));
+    }
+    // entries past the part (the last thread of the row's end) are dropped
+#pragma unroll
+    for (int w = 0; w < (SUNR + 7) / 8; ++w) {
+      const int keep = nmine - 32 * w;
+      m[w] &= keep >= 32 ? 0xFFFFFFFFu : (keep <= 0 ? 0u : (1u << keep) - 1u);
+    }
+    int cl = 0;
+#pragma unroll
+    for (int w = 0; w < (SUNR + 7) / 8; ++w) cl += __popc(m[w]);
     int tot;
-    const int ex = block_exclusive_scan(v, sm.scr.warp_sums, STHREADS, tot, tid, BlockSync());
-    if (c0 + tid < nc) sm.coff[c0 + tid] = run + ex;
+    // (its barriers also keep every thread's reads of buf ahead of the next pass's copies)
+    int off = run + block_exclusive_scan(cl, sm.scr.warp_sums, STHREADS, tot, tid, BlockSync());
+#pragma unroll
+    for (int w = 0; w < (SUNR + 7) / 8; ++w) {
+      for (uint32_t mw = m[w]; mw != 0u; mw &= mw - 1u, ++off) {
+        const int i = 32 * w + __ffs(mw) - 1;
+        if (off < FCAP) {
+          sm.key[off] = float_key(sm.buf[t0 + i]);
+          sm.pos[off] = base + t0 + i;
+        }
+      }
+    }
     run += tot;
+    ok = __syncthreads_and(ok);                  // one decision for the CTA
+    if (!ok) break;
   }
-  if (tid == 0) sm.coff[nc] = run;
-  __syncthreads();
-  if (run != ncand) {                            // counts disagree with the histogram: take the general path
-    radix_select_row(sc, n, k, out);
-    return;
+  if (tid == 0) sm.count = ok ? run : -1;        // a CTA whose copy gave up sends the row to the radix path
+  cluster.sync();                                // every CTA's list and count are complete
+  // this CTA's list goes to CTA 0's, after the lists of the CTAs before it
+  int before = 0, total = 0;
+#pragma unroll
+  for (int r = 0; r < SCL; ++r) {
+    const int c = r == rank ? sm.count : *cluster.map_shared_rank(&sm.count, r);
+    if (c < 0) total = -1 << 30;
+    if (r < rank) before += c;
+    total += c;
   }
-  // a warp per chunk: its (position, key) lists are read coalesced, in order
-  const int* crand = cand + static_cast<size_t>(row) * nch * CH;
-  const uint32_t* crandk = candk + static_cast<size_t>(row) * nch * CH;
-  for (int c = tid >> 5; c < nc; c += SWARPS) {
-    const int base = sm.coff[c], nci = sm.coff[c + 1] - base;
-    for (int i = tid & 31; i < nci; i += 32) {
-      sm.pos[base + i] = crand[static_cast<size_t>(c) * CH + i];
-      sm.key[base + i] = crandk[static_cast<size_t>(c) * CH + i];
+  const bool good = total == ncand;              // then every count is within FCAP too
+  if (good && rank > 0) {
+    uint32_t* dk = cluster.map_shared_rank(sm.key, 0);
+    int* dp = cluster.map_shared_rank(sm.pos, 0);
+    for (int i = tid; i < sm.count; i += STHREADS) {
+      dk[before + i] = sm.key[i];
+      dp[before + i] = sm.pos[i];
     }
   }
-  __syncthreads();
+  cluster.sync();                                // CTA 0 holds every list
+  if (!ok && tid == 0) tc::mbar_wait(&sm.bar, phase, nullptr);
+  if (rank != 0) return;
+  if (!good) {                                   // lists disagree with the histogram: the general path
+    radix_select_row(sc, n, k, out);
+    return;
+  }
   if (ncand > k) {
     uint32_t thr;
-    // the candidates above the threshold bin (its histogram count tells how
-    // many) are all kept; only the bin's own keys are cut
-    const uint32_t lo_key = static_cast<uint32_t>(sm.bsel) << (32 - kDecHistBits);
-    const uint32_t hi_key = lo_key | ((1u << (32 - kDecHistBits)) - 1u);
-    const int above = ncand - hist[static_cast<size_t>(row) * HBINS + sm.bsel];
-    cut_list<STHREADS, FSEG>(sm.key, sm.pos, ncand, k, k, lo_key, hi_key, &sm.scr, tid, BlockSync(), &thr, above);
+    const uint32_t hi_key = lo | ((1u << (32 - kDecHistBits)) - 1u);
+    const int above = ncand - hrow[sm.bsel];
+    cut_list<STHREADS, FSEG>(sm.key, sm.pos, ncand, k, k, lo, hi_key, &sm.scr, tid, BlockSync(), &thr, above);
   }
   for (int j = tid; j < k; j += STHREADS) out[j] = sm.pos[j];
 }
@@ -617,21 +644,15 @@ __global__ void __launch_bounds__(256) zero_words_kernel(uint4* p, size_t n16) {
     p[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
-cudaError_t launch_chunked_select(const DecWs& d, const IndexerArgs& a, cudaStream_t st) {
+cudaError_t launch_cluster_select(const DecWs& d, const IndexerArgs& a, int* dev_status, cudaStream_t st) {
   const int n = a.q_pos0 + 1;                    // one row per sequence (T = 1)
-  if (n > a.k) {
-    dim3 g1((n + CH - 1) / CH, a.B);
-    const cudaError_t e = launch_pdl(select_chunk_kernel, g1, dim3(CTHREADS), 0, st, d.scores, d.pitch,
-                                     static_cast<const int*>(d.hist), d.cnt, d.cand, d.candk, d.nch, n, a.k);
-    if (e != cudaSuccess) return e;
-  }
-  const size_t smem = sizeof(FinishSmem);
-  cudaError_t e = cudaFuncSetAttribute(select_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  const size_t smem = sizeof(ClusterSelSmem);
+  const cudaError_t e = cudaFuncSetAttribute(select_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(select_finish_kernel, dim3(a.B), dim3(STHREADS), smem, st, static_cast<const float*>(d.scores),
-                    d.pitch, static_cast<const int*>(d.hist), static_cast<const int*>(d.cnt),
-                    static_cast<const int*>(d.cand), static_cast<const uint32_t*>(d.candk), d.nch, a.idx, n, a.k);
+  return launch_pdl(select_cluster_kernel, dim3(SCL, a.B), dim3(STHREADS), smem, st,
+                    static_cast<const float*>(d.scores), d.pitch, static_cast<const int*>(d.hist), a.idx, n, a.k,
+                    dev_status);
 }
 
 template <int D>
@@ -667,7 +688,7 @@ cudaError_t launch_indexer_decode(const IndexerArgs& a, void* ws, size_t ws_byte
     size_t need = 0;
     const DecWs d = carve_ws(ws, a.B * a.T, a.S, &need);
     if (ws_bytes >= need) {
-      // histogram built by the scorer, then the chunked select
+      // histogram built by the scorer, then the clustered select
       // rows * HBINS ints: a whole number of 16-byte words (HBINS is a multiple of 4)
       const size_t n16 = static_cast<size_t>(a.B) * a.T * HBINS / 4;
       e = launch_pdl(zero_words_kernel, dim3(static_cast<unsigned>((n16 + 255) / 256 < 148 ? (n16 + 255) / 256 : 148)),
@@ -675,7 +696,7 @@ cudaError_t launch_indexer_decode(const IndexerArgs& a, void* ws, size_t ws_byte
       if (e != cudaSuccess) return e;
       e = launch_indexer_decode_tc(a, scores, pitch, d.hist, dev_status, st);
       if (e != cudaSuccess) return e;
-      return launch_chunked_select(d, a, st);
+      return launch_cluster_select(d, a, dev_status, st);
     }
     e = launch_indexer_decode_tc(a, scores, pitch, nullptr, dev_status, st);
     if (e != cudaSuccess) return e;

@@ -170,6 +170,9 @@ indexer_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
     if (lane == 0) {
       tc::tma_prefetch_map(&tm_q);
       tc::tma_prefetch_map(&tm_k);
+      // every key is read once: its lines go first when L2 needs room, so the
+      // stream does not push out the score rows the select reads next
+      const uint64_t pol_k = tc::l2_evict_first();
       bool ok = true;
       int nseq = 0, cur_b = -1, issued_k = 0, issued_q = 0;
       int b = static_cast<int>(u0 / ntile), kt = static_cast<int>(u0 % ntile);
@@ -189,11 +192,11 @@ indexer_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
         if (!tc::mbar_wait(&sm.kempty[s], ((i / nst) & 1) ^ 1, &sm.abort)) { ok = false; break; }
         if (e4m3) {
           tc::mbar_arrive_expect_tx(&sm.kfull[s], RAW_TILE);
-          tc::tma_load_2d(sm.kst + s * RAW_TILE, &tm_k, &sm.kfull[s], 0, krow);
+          tc::tma_load_2d_hint(sm.kst + s * RAW_TILE, &tm_k, &sm.kfull[s], 0, krow, pol_k);
         } else {
           tc::mbar_arrive_expect_tx(&sm.kfull[s], BF_TILE);
-          tc::tma_load_2d(sm.kst + s * BF_TILE, &tm_k, &sm.kfull[s], 0, krow);
-          tc::tma_load_2d(sm.kst + s * BF_TILE + KT * 128, &tm_k, &sm.kfull[s], 64, krow);
+          tc::tma_load_2d_hint(sm.kst + s * BF_TILE, &tm_k, &sm.kfull[s], 0, krow, pol_k);
+          tc::tma_load_2d_hint(sm.kst + s * BF_TILE + KT * 128, &tm_k, &sm.kfull[s], 64, krow, pol_k);
         }
         issued_k = i + 1;
       }

@@ -118,10 +118,8 @@ def test_workspace_sizes(lib):
     assert B.workspace_size(B.make_dims(1, 8192, 8192, 64, 128, 2048, 32, 128)) == 0
     ws = B.workspace_size(B.make_dims(32, 1, 131073, 64, 128, 2048, 32, 128, q_pos0=131072))
     pitch = (131073 + 3) // 4 * 4
-    # score rows, plus the chunked select's key histogram (2048 bins) and
-    # candidate positions (one int per score slot, rounded to 4096-score chunks)
-    chunks = (pitch + 4095) // 4096
-    assert ws >= 32 * pitch * 4 + 32 * 2048 * 4 + 32 * chunks * 4096 * 4
+    # score rows, plus the clustered select's key histogram (2048 bins per row)
+    assert ws >= 32 * pitch * 4 + 32 * 2048 * 4
     # and the split decode attention's partial states (32 rows x 16 splits)
     assert ws >= 32 * 16 * (2 * 32 + 32 * 128) * 4
     with pytest.raises(ValueError):

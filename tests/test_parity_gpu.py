@@ -292,7 +292,7 @@ def test_decode_select_ties(S, n_top, top_val):
 
 
 def test_decode_select_paths_agree():
-    # the chunked select (workspace with histogram and candidate buffers) and
+    # the clustered select (workspace with the histogram) and
     # the one-CTA select (workspace of the score rows only) pick the same rows
     dc = synth.DECODE.with_(B=3)
     S = 40000

@@ -10,8 +10,9 @@ this test checks, through the C ABI:
   leaves different scores in the shared array, and both calls give exactly
   the indices of ic_indexer_topk with a caller workspace;
 * one case on integer inputs is exact against the CPU oracle as well;
-* a case near the array's limit (the score rows fit, the chunked select's
-  buffers do not) takes the select path that histograms the score row itself;
+* a case near the array's limit (the score rows fit, the score-key
+  histogram of the clustered select does not) takes the select path that
+  histograms the score row itself;
 * sizes past the array are refused without touching the output.
 
 Kept in its own file, collected last, so a failure here never hides the
@@ -55,7 +56,7 @@ CASES = [
     # B, T, S, S_cap, q_pos0, k, key dtype, seed
     (8, 1, 30001, 30100, 30000, 2048, "e4m3", 11),
     (3, 2, 9002, 9002, 9000, 512, "bf16", 12),
-    (32, 1, 250000, 250000, 249999, 2048, "e4m3", 15),   # score rows fill most of the array
+    (32, 1, 261000, 261000, 260999, 2048, "e4m3", 15),   # the score rows fit, the histogram does not
 ]
 
 
