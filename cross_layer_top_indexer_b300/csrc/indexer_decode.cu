@@ -526,26 +526,11 @@ select_cluster_kernel(const float* scores, size_t pitch, const int* hist, int32_
       for (int j = tid; j < k; j += STHREADS) out[j] = j < n ? j : -1;
     return;
   }
-  const int* hrow = hist + static_cast<size_t>(row) * HBINS;
-  threshold_bin<STHREADS>(hrow, k, sm.scr.warp_sums, &sm.bsel, &sm.ncand);   // ends with a CTA barrier
-  const int ncand = sm.ncand;
-  if (ncand > FCAP) {
-    if (rank == 0) radix_select_row(sc, n, k, out);
-    return;
-  }
   // this CTA's part of the row (a multiple of 4 scores, so copies stay 16-byte aligned)
-  const uint32_t lo = static_cast<uint32_t>(sm.bsel) << (32 - kDecHistBits);
   const int part = ((n + SCL - 1) / SCL + 3) & ~3;
   const int p0 = min(n, rank * part), p1 = min(n, p0 + part);
-  // Thread t lists the scores [4 SUNR t, 4 SUNR (t + 1)) of each pass, so
-  // the pass's position order is the thread order.  A thread marks its
-  // candidates in a bit mask as it reads them (independent 16-byte reads,
-  // 272 bytes apart: distinct banks within each 8-thread phase) and then
-  // visits only the marked ones, about 2 of its 68 scores on average.
-  int run = 0;
-  bool ok = true;
-  uint32_t phase = 0;
-  for (int base = p0; base < p1; base += SPASS, phase ^= 1u) {
+  // a pass's scores into buf, by bulk copies (thread 0)
+  auto issue = [&](int base) {
     if (tid == 0) {
       // up to the row's pitch, which holds n rounded up to 4 scores
       const uint32_t bytes = static_cast<uint32_t>(((min(p1 - base, SPASS) + 3) & ~3) * sizeof(float));
@@ -555,6 +540,30 @@ select_cluster_kernel(const float* scores, size_t pitch, const int* hist, int32_
         tc::bulk_g2s(reinterpret_cast<char*>(sm.buf) + off, reinterpret_cast<const char*>(sc + base) + off,
                      min(static_cast<uint32_t>(SPIECE), bytes - off), &sm.bar);
     }
+  };
+  if (p0 < p1) issue(p0);                        // the first pass lands while the threshold is found
+  const int* hrow = hist + static_cast<size_t>(row) * HBINS;
+  threshold_bin<STHREADS>(hrow, k, sm.scr.warp_sums, &sm.bsel, &sm.ncand);   // ends with a CTA barrier
+  const int ncand = sm.ncand;
+  if (ncand > FCAP) {
+    if (p0 < p1 && tid == 0) tc::mbar_wait(&sm.bar, 0, nullptr);   // no copy may land after the exit
+    if (rank == 0) radix_select_row(sc, n, k, out);
+    return;
+  }
+  // key(x) >= lo  <=>  x >= lo_f for every score that is not a NaN (a NaN
+  // key would make the lists disagree with the histogram: radix path)
+  const uint32_t lo = static_cast<uint32_t>(sm.bsel) << (32 - kDecHistBits);
+  const float lo_f = key_float(lo);
+  // Thread t lists the scores [4 SUNR t, 4 SUNR (t + 1)) of each pass, so
+  // the pass's position order is the thread order.  A thread marks its
+  // candidates in a bit mask as it reads them (independent 16-byte reads,
+  // 272 bytes apart: distinct banks within each 8-thread phase) and then
+  // visits only the marked ones, about 2 of its 68 scores on average.
+  int run = 0;
+  bool ok = true;
+  uint32_t phase = 0;
+  for (int base = p0; base < p1; base += SPASS, phase ^= 1u) {
+    if (base != p0) issue(base);
     if (!tc::mbar_wait(&sm.bar, phase, nullptr)) {
       ok = false;                                // a copy may still land: waited for again before the exit
       if (status) atomicExch(status, kDevTimeout);
@@ -566,8 +575,8 @@ select_cluster_kernel(const float* scores, size_t pitch, const int* hist, int32_
 #pragma unroll
     for (int j = 0; j < SUNR; ++j) {
       const float4 x = mine[j];
-      const uint32_t f = (float_key(x.x) >= lo ? 1u : 0u) | (float_key(x.y) >= lo ? 2u : 0u) |
-                         (float_key(x.z) >= lo ? 4u : 0u) | (float_key(x.w) >= lo ? 8u : 0u);
+      const uint32_t f = (x.x >= lo_f ? 1u : 0u) | (x.y >= lo_f ? 2u : 0u) | (x.z >= lo_f ? 4u : 0u) |
+                         (x.w >= lo_f ? 8u : 0u);
       m[j >> 3] |= f << (4 * (j & 7));
     }
     // entries past the part (the last thread of the row's end) are dropped
