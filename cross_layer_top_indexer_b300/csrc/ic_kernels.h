@@ -70,11 +70,17 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, void* ws, size_t ws_bytes, int
 // Tensor-core (tcgen05 + TMA gather) kernel for Hq = 32, Dh = 128 and many rows:
 // The tcgen05 attention: 0 when it does not take these shapes, 1 for whole
 // rows per CTA, n > 1 when each row is shared among n CTAs (few rows, e.g.
-// decode), which then write per-share partials (max, sum, unnormalised O;
-// the split kernel's layout) for the combine kernel.
+// decode), whose per-share partials (max, sum, unnormalised O; the split
+// kernel's layout) are merged in a thread block cluster or by the combine
+// kernel.
 constexpr int kTcTargetCtas = 148;
 int sparse_attn_tc_splits(const AttnArgs& a);
+// nsplit > 1 with partials == nullptr: the shares of a row run as one thread
+// block cluster and are merged in it (sparse_attn_tc_cluster_merge says when
+// that launch is possible); otherwise they go to `partials`.
 cudaError_t launch_sparse_attn_tc(const AttnArgs& a, int nsplit, float* partials, int* dev_status, cudaStream_t st);
+constexpr int kTcMaxClusterSplit = 8;   // portable cluster size
+bool sparse_attn_tc_cluster_merge(const AttnArgs& a, int nsplit);
 
 // Per-row overlap |I_a ∩ I_b| / k of two index tensors [R, k] (count optional).
 cudaError_t launch_overlap(int R, int k, const int32_t* ia, const int32_t* ib, float* ratio, int32_t* count,

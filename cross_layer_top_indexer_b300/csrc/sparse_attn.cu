@@ -406,7 +406,10 @@ cudaError_t launch_sparse_attn(const AttnArgs& a, void* ws, size_t ws_bytes, int
   const int tsplit = sparse_attn_tc_splits(a);
   if (tsplit == 1) return launch_sparse_attn_tc(a, 1, nullptr, dev_status, st);
   if (tsplit > 1) {
-    // each row shared among tsplit CTAs of the tcgen05 kernel, then merged
+    // each row shared among tsplit CTAs of the tcgen05 kernel, then merged:
+    // inside the launch (one cluster per row) when the shares fit one per
+    // CTA, else by the combine kernel
+    if (sparse_attn_tc_cluster_merge(a, tsplit)) return launch_sparse_attn_tc(a, tsplit, nullptr, dev_status, st);
     const int rows = a.B * a.T;
     if ((size_t)rows * tsplit * Partial::floats(DHMAX) * sizeof(float) > ws_bytes) return cudaErrorInvalidValue;
     cudaError_t e = launch_sparse_attn_tc(a, tsplit, reinterpret_cast<float*>(ws), dev_status, st);

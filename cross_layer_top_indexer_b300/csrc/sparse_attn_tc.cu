@@ -20,9 +20,13 @@
 // scores, and the output accumulates in TMEM with d on the lanes.
 //
 // Persistent CTAs (one per SM) walk work items item = blockIdx.x + i*gridDim.x:
-// whole query rows, or, with few rows (decode), a range of a row's tiles, in
-// which case the CTA writes the share's reference max, sum and unnormalised O
-// and a combine kernel merges the shares of a row.
+// whole query rows, or, with few rows (decode), a range of a row's tiles.  A
+// share of a row ends with its reference max, sum and unnormalised O.  When
+// the shares fit one per CTA, the CTAs of a row are launched as one thread
+// block cluster: each stages its share in shared memory and, after the
+// cluster barrier, CTA r merges heads [r HQ/n, (r+1) HQ/n) of the row from
+// all the shares through distributed shared memory and writes O.  Otherwise
+// the shares go to a workspace and a combine kernel merges them.
 // Warp roles (14 warps):
 //   warps 0-7  softmax + epilogue in two head groups: warps 0-3 own heads
 //              0-15, warps 4-7 heads 16-31 (warp w reads TMEM lane quarter
@@ -70,6 +74,7 @@
 // Every wait is bounded; a wait that gives up sets the CTA's abort flag and
 // the device status word, every role winds down, in-flight MMAs and copies
 // are waited for (bounded), and tensor memory is released before returning.
+#include <cooperative_groups.h>
 #include <math.h>
 
 #include "ic_common.cuh"
@@ -419,7 +424,15 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
         for (int h = 0; h < HG; ++h) Ob[h * DH] = __float2bfloat16_rn(__uint_as_float(o[h]) * sm.inv_l[mb][h0 + h]);
       } else {
         // a share of a row: (reference max, sum, unnormalised O) per head,
-        // merged with the row's other shares by the combine kernel
+        // merged with the row's other shares in the cluster (O staged in
+        // the ring, free once the last PV is complete; the max and the sum
+        // stay in m_fin / l_fin) or by the combine kernel
+        if (partials == nullptr) {
+          float* so = reinterpret_cast<float*>(sm.ring[0]) + static_cast<size_t>(h0) * DH + my_lane;
+#pragma unroll
+          for (int h = 0; h < HG; ++h) so[h * DH] = __uint_as_float(o[h]);
+          return true;
+        }
         float* pb = partials + static_cast<size_t>(item_of(m)) * (2 * HQ + HQ * DH);
         if (gw == 0 && lane < HG) {
           pb[h0 + lane] = sm.m_fin[mb][h0 + lane];
@@ -564,6 +577,48 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   __syncthreads();
   tc::tc_fence_after();
   if (warp == MMA_WARP) tc::tmem_dealloc(tmem, TMEM_COLS);
+  if constexpr (kSplit) {
+    if (partials == nullptr) {
+      // one item per CTA, the row's nsplit CTAs are this cluster (rank = share)
+      namespace cg = cooperative_groups;
+      cg::cluster_group cluster = cg::this_cluster();
+      cluster.sync();                            // every share is staged
+      const int rank = static_cast<int>(cluster.block_rank());
+      const int row = item_row(0);
+      const int hpc = (HQ + nsplit - 1) / nsplit;
+      const int hb = min(HQ, rank * hpc), he = min(HQ, hb + hpc);
+      __nv_bfloat16* Ob = reinterpret_cast<__nv_bfloat16*>(a.O) + static_cast<size_t>(row) * HQ * DH;
+      for (int e = hb * DH + tid; e < he * DH; e += NTHREADS) {
+        const int h = e / DH;
+        // every share's values are requested before any is used (one round
+        // trip through the cluster instead of one per share)
+        float mv[kTcMaxClusterSplit], lv[kTcMaxClusterSplit], ov[kTcMaxClusterSplit];
+#pragma unroll
+        for (int r = 0; r < kTcMaxClusterSplit; ++r) {
+          if (r < nsplit) {
+            mv[r] = *cluster.map_shared_rank(&sm.m_fin[0][h], r);
+            lv[r] = *cluster.map_shared_rank(&sm.l_fin[0][h], r);
+            ov[r] = *cluster.map_shared_rank(reinterpret_cast<float*>(sm.ring[0]) + e, r);
+          }
+        }
+        float M = -INFINITY;
+#pragma unroll
+        for (int r = 0; r < kTcMaxClusterSplit; ++r)
+          if (r < nsplit) M = fmaxf(M, mv[r]);
+        float l = 0.0f, acc = 0.0f;
+#pragma unroll
+        for (int r = 0; r < kTcMaxClusterSplit; ++r) {
+          if (r < nsplit) {
+            const float f = exp2f(mv[r] - M);
+            l += lv[r] * f;
+            acc += ov[r] * f;
+          }
+        }
+        Ob[e] = __float2bfloat16_rn(l > 0.0f ? acc / l : 0.0f);
+      }
+      cluster.sync();                            // no other CTA reads this one's shares any more
+    }
+  }
 }
 
 }  // namespace
@@ -587,7 +642,7 @@ int sparse_attn_tc_splits(const AttnArgs& a) {
 cudaError_t launch_sparse_attn_tc(const AttnArgs& a, int nsplit, float* partials, int* dev_status, cudaStream_t st) {
   CUtensorMap tm_q, tm_k, tm_v;
   const uint64_t rows = static_cast<uint64_t>(a.B) * a.T;
-  if (nsplit < 1 || (nsplit > 1 && partials == nullptr)) return cudaErrorInvalidValue;
+  if (nsplit < 1) return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&tm_q, a.Q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, rows * HQ, DH, HQ, 64))
     return cudaErrorInvalidValue;
   if (!encode_tmap_2d(&tm_k, a.K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, static_cast<uint64_t>(a.B) * a.S_cap, DH, 1,
@@ -605,7 +660,34 @@ cudaError_t launch_sparse_attn_tc(const AttnArgs& a, int nsplit, float* partials
   if (e != cudaSuccess) return e;
   const uint64_t items = rows * static_cast<uint64_t>(nsplit);
   const int grid = static_cast<int>(items < static_cast<uint64_t>(n_sm) ? items : n_sm);
+  if (nsplit > 1 && partials == nullptr) {
+    // one share per CTA, the shares of a row as one cluster, merged in it
+    if (items > static_cast<uint64_t>(n_sm) || nsplit > kTcMaxClusterSplit) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(items));
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(nsplit);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, sparse_attn_tc_kernel<true>, tm_q, tm_k, tm_v, a, nsplit, partials, dev_status);
+  }
   return launch_pdl(kern, dim3(grid), dim3(NTHREADS), smem, st, tm_q, tm_k, tm_v, a, nsplit, partials, dev_status);
+}
+
+bool sparse_attn_tc_cluster_merge(const AttnArgs& a, int nsplit) {
+  int dev = 0, n_sm = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+  const long long items = static_cast<long long>(a.B) * a.T * nsplit;
+  return nsplit > 1 && nsplit <= kTcMaxClusterSplit && items <= n_sm;
 }
 
 }  // namespace ic
