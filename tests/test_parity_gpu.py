@@ -382,9 +382,12 @@ def _attn_case(Bn, T, S, S_cap, k, mode, seed):
     (6, 1, 3000, 3000, 512, "masked_head"),   # an empty first chunk, empty rows, out-of-range slots
     (3, 1, 4000, 4000, 1152, "growing"),      # 9 tiles of 128 keys shared 3 + 3 + 3 among CTAs
     (7, 1, 2500, 2600, 644, "spike"),         # 6 tiles, the last with 4 keys, shared 2 + 2 + 2
+    (8, 1, 3000, 3000, 2048, "growing"),      # 16 tiles shared by a cluster of 8 CTAs, 2 each
+    (30, 2, 2500, 2500, 2048, "normal"),      # 60 rows: clusters of 2 CTAs, 8 tiles each
 ])
 def test_decode_attention_split_cases(Bn, T, S, S_cap, k, mode):
     # few rows: the k positions are split across CTAs and the splits merged
+    # (in a thread block cluster per row: clusters of 2, 3, 4 and 8 CTAs here)
     Q, K, V, idx = _attn_case(Bn, T, S, S_cap, k, mode, 19)
     O = B.sparse_attn(Q, K, V, idx, S=S)
     torch.cuda.synchronize()
