@@ -218,8 +218,14 @@ IC_EXPORT ic_status ic_sparse_attn(int B, int T, int S, int S_cap, int Hq, int D
   if (st != IC_OK) return st;
   if (!(scale >= 0.0f)) return fail(IC_ERR_ARG, "scale must be >= 0");
   if (scale == 0.0f) scale = 1.0f / sqrtf((float)Dh);
-  ic::AttnArgs a{Q, K, V, idx, O, B, T, S, S_cap, Hq, Dh, k, scale};
+  ic::AttnArgs a{Q, K, V, idx, O, B, T, S, S_cap, Hq, Dh, k, scale, 0};
   return run_attn(a, ws, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+// Do the byte ranges [a, a + na) and [b, b + nb) share a byte?
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
 }
 
 static ic_status forward_impl(const char* pattern, int n_layers, const ic_layer* layers, const ic_dims* dims,
@@ -280,7 +286,17 @@ static ic_status forward_impl(const char* pattern, int n_layers, const ic_layer*
       if (ev) cudaEventRecord(ev[4 * l + 1], st);
       ++calls;
     }
-    ic::AttnArgs a{L.Q, L.K, L.V, index_cache, L.O, d.B, d.T, d.S, d.S_cap, d.Hq, d.Dh, d.k, scale};
+    ic::AttnArgs a{L.Q, L.K, L.V, index_cache, L.O, d.B, d.T, d.S, d.S_cap, d.Hq, d.Dh, d.k, scale, 0};
+    // a Shared layer's attention follows the previous layer's, which writes
+    // only that layer's O: unless that O overlaps this layer's inputs, they
+    // are complete when the launch starts
+    if (pattern[l] == 'S' && l > 0) {
+      const size_t q_bytes = (size_t)d.B * d.T * d.Hq * d.Dh * 2, kv_bytes = (size_t)d.B * d.S_cap * d.Dh * 2;
+      const void* po = layers[l - 1].O;
+      a.inputs_ready = !overlaps(po, q_bytes, L.Q, q_bytes) && !overlaps(po, q_bytes, L.K, kv_bytes) &&
+                       !overlaps(po, q_bytes, L.V, kv_bytes) &&
+                       !overlaps(po, q_bytes, index_cache, (size_t)d.B * d.T * d.k * 4);
+    }
     if (ev) cudaEventRecord(ev[4 * l + 2], st);
     ic_status r = run_attn(a, ws, ws_bytes, st);
     if (r != IC_OK) { if (indexer_calls) *indexer_calls = calls; return r; }

@@ -29,6 +29,12 @@ struct AttnArgs {
   void* O;               // [B,T,Hq,Dh] bf16
   int B, T, S, S_cap, Hq, Dh, k;
   float scale;
+  // Nonzero: Q, K, V and idx are not written by the kernel just before this
+  // launch on the stream, and everything before that kernel has completed,
+  // so the tensor-core kernel reads them before its programmatic-launch wait
+  // (it still waits before writing O).  Set for the Shared layers of a
+  // forward, whose launch follows the previous layer's attention.
+  int inputs_ready;
 };
 
 // Fused prefill indexer + streaming top-k (scores never leave the SM).

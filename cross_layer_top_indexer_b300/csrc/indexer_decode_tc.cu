@@ -160,9 +160,12 @@ indexer_decode_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
-  // the set-up above may overlap the kernel before; the keys, q, w and scales
-  // are read only once it has completed
-  grid_dep_wait();
+  // The set-up above may overlap the kernel before.  With a histogram, that
+  // kernel is the histogram clear, which writes nothing else and started
+  // only once everything before it had completed: the roles that never
+  // touch the histogram read the keys, q, w and scales at once, and only
+  // the epilogue waits.  Without one, every role waits.
+  if (hist == nullptr || warp >= 4) grid_dep_wait();
   grid_dep_trigger();
 
   if (warp == 0) {

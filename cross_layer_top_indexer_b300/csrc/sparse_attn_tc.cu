@@ -237,9 +237,12 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
-  // the set-up above may overlap the kernel before; Q, the index rows and K/V
-  // are read only once it has completed
-  grid_dep_wait();
+  // The set-up above may overlap the kernel before.  Q, the index rows and
+  // K/V are read once it has completed, or at once when the caller knows
+  // that kernel does not write them (inputs_ready); O is written only after
+  // it has completed either way.
+  const bool early = a.inputs_ready != 0;
+  if (!early) grid_dep_wait();
   grid_dep_trigger();
   const uint32_t tmem = sm.tmem_base;
   const uint32_t tS = tmem;          // columns 0..63: S buffers
@@ -394,6 +397,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     // at the next row's first tile (after that tile's P is handed over), so
     // the softmax never waits for the PV pipeline to drain at a row boundary.
     auto finish_row = [&](int m) -> bool {
+      if (early) grid_dep_wait();
       const int mb = m & 1;
       const bool w_ok = tc::mbar_wait<kWaitHintNs>(&sm.ofull[mb], (m >> 1) & 1, &sm.abort);
       if (tc::named_sync_or(bar_id, GROUP_THREADS, !w_ok || sm.abort)) return false;
@@ -583,6 +587,7 @@ sparse_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
       namespace cg = cooperative_groups;
       cg::cluster_group cluster = cg::this_cluster();
       cluster.sync();                            // every share is staged
+      if (early) grid_dep_wait();
       const int rank = static_cast<int>(cluster.block_rank());
       const int row = item_row(0);
       const int hpc = (HQ + nsplit - 1) / nsplit;
