@@ -495,6 +495,94 @@ __device__ void threshold_bin(const int* h, int k, int* warp_sums, int* s_bsel, 
   __syncthreads();
 }
 
+// The bin b of h[0 .. NB) (NB / STHREADS consecutive bins per thread) where
+// the count from the top reaches `need`: count(bins > b) < need <= count(bins
+// >= b); *rem = need - count(bins > b).  All STHREADS threads call it.
+template <int NB>
+__device__ void top_down_bin(const int* h, int need, SelectScratch* scr, int* bin, int* rem) {
+  constexpr int BPT = NB / STHREADS;
+  const int tid = threadIdx.x;
+  int c[BPT];
+  int sum = 0;
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) { c[j] = h[NB - 1 - BPT * tid - j]; sum += c[j]; }
+  int total;
+  const int excl = block_exclusive_scan(sum, scr->warp_sums, STHREADS, total, tid, BlockSync());
+  if (excl < need && need <= excl + sum) {
+    int cum = excl;
+#pragma unroll
+    for (int j = 0; j < BPT; ++j) {
+      if (cum + c[j] >= need) { scr->sel_digit = NB - 1 - BPT * tid - j; scr->sel_need = need - cum; break; }
+      cum += c[j];
+    }
+  }
+  __syncthreads();
+  *bin = scr->sel_digit;
+  *rem = scr->sel_need;
+  __syncthreads();
+}
+
+// Exactly k of the n candidates (key[i], pos[i]), i in position order, to
+// out in that order: the `above` entries over the threshold bin [lo, lo +
+// 2^21) (fewer than k) and the best k - above of the bin's own entries, ties
+// to the lower position.  Two histograms of the 21 bits under the bin's
+// (2048 bins of the upper 11, then 1024 of the lower 10 within the chosen
+// one) give the exact threshold key; one ordered pass writes the
+// positions.  h: scratch of 2048 ints.  All STHREADS threads call it.
+__device__ void cut_bin_to_out(const uint32_t* key, const int* pos, int n, int k, uint32_t lo, int above, int* h,
+                               SelectScratch* scr, int32_t* out) {
+  constexpr int LOW = 32 - kDecHistBits;
+  constexpr int BB = 10, NA = 1 << (LOW - BB), NB = 1 << BB;
+  static_assert(NA % STHREADS == 0 && NB % STHREADS == 0, "bins per thread");
+  const int tid = threadIdx.x;
+  const uint32_t hi = lo | ((1u << LOW) - 1u);
+  const int seg = (n + STHREADS - 1) / STHREADS;
+  const int i0 = min(n, tid * seg), i1 = min(n, i0 + seg);
+  // the upper 11 bits
+  for (int b = tid; b < NA; b += STHREADS) h[b] = 0;
+  __syncthreads();
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t kk = key[i];
+    if (kk <= hi) atomicAdd(&h[(kk - lo) >> BB], 1);   // every candidate has kk >= lo
+  }
+  __syncthreads();
+  int ba, need_a;
+  top_down_bin<NA>(h, k - above, scr, &ba, &need_a);
+  // the lower 10 bits, within bin ba
+  const uint32_t lo_a = lo + (static_cast<uint32_t>(ba) << BB), hi_a = lo_a + (NB - 1);
+  for (int b = tid; b < NB; b += STHREADS) h[b] = 0;
+  __syncthreads();
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t kk = key[i];
+    if (kk >= lo_a && kk <= hi_a) atomicAdd(&h[kk - lo_a], 1);
+  }
+  __syncthreads();
+  int bb, eq_keep;
+  top_down_bin<NB>(h, need_a, scr, &bb, &eq_keep);
+  const uint32_t thr = lo_a + static_cast<uint32_t>(bb);
+  // keep key > thr, and the first eq_keep entries with key == thr
+  int n_eq = 0;
+  for (int i = i0; i < i1; ++i) n_eq += key[i] == thr;
+  int eq_total;
+  int eq_rank = block_exclusive_scan(n_eq, scr->warp_sums, STHREADS, eq_total, tid, BlockSync());
+  int n_keep = 0;
+  for (int i = i0, e = eq_rank; i < i1; ++i) {
+    const uint32_t kk = key[i];
+    n_keep += kk > thr || (kk == thr && e++ < eq_keep);
+  }
+  int tot;
+  int off = block_exclusive_scan(n_keep, scr->warp_sums, STHREADS, tot, tid, BlockSync());
+  for (int i = i0, e = eq_rank; i < i1; ++i) {
+    const uint32_t kk = key[i];
+    if (kk > thr || (kk == thr && e++ < eq_keep)) {
+      if (off < k) out[off] = pos[i];
+      ++off;
+    }
+  }
+  // (tot == k whenever the lists agree with the histogram, as the caller checked)
+  for (int j = tot + tid; j < k; j += STHREADS) out[j] = -1;
+}
+
 struct __align__(128) ClusterSelSmem {
   float buf[SPASS];                      // a pass of this CTA's part of the score row
   uint32_t key[FCAP];
@@ -632,13 +720,10 @@ select_cluster_kernel(const float* scores, size_t pitch, const int* hist, int32_
     radix_select_row(sc, n, k, out);
     return;
   }
-  if (ncand > k) {
-    uint32_t thr;
-    const uint32_t hi_key = lo | ((1u << (32 - kDecHistBits)) - 1u);
-    const int above = ncand - hrow[sm.bsel];
-    cut_list<STHREADS, FSEG>(sm.key, sm.pos, ncand, k, k, lo, hi_key, &sm.scr, tid, BlockSync(), &thr, above);
-  }
-  for (int j = tid; j < k; j += STHREADS) out[j] = sm.pos[j];
+  if (ncand > k)
+    cut_bin_to_out(sm.key, sm.pos, ncand, k, lo, ncand - hrow[sm.bsel], reinterpret_cast<int*>(sm.buf), &sm.scr, out);
+  else
+    for (int j = tid; j < k; j += STHREADS) out[j] = sm.pos[j];
 }
 
 // Clears the score histograms before the scorer adds into them.  A kernel
