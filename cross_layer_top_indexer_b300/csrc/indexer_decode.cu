@@ -738,6 +738,29 @@ __global__ void __launch_bounds__(256) zero_words_kernel(uint4* p, size_t n16) {
     p[i] = make_uint4(0u, 0u, 0u, 0u);
 }
 
+// Whether clusters of SCL CTAs with the clustered select's shared memory fit
+// the device (asked once per process; otherwise the one-CTA select runs).
+bool cluster_select_ok() {
+  static int ok = -1;
+  if (ok < 0) {
+    int v = 0, n = 0;
+    const size_t smem = sizeof(ClusterSelSmem);
+    cudaError_t q = cudaFuncSetAttribute(select_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (q == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(SCL, 1);
+      cfg.blockDim = dim3(STHREADS);
+      cfg.dynamicSmemBytes = smem;
+      q = cudaOccupancyMaxActiveClusters(&n, select_cluster_kernel, &cfg);
+      if (q == cudaSuccess && n > 0) v = 1;
+    }
+    if (q != cudaSuccess) cudaGetLastError();    // a refused query leaves no error behind
+    ok = v;
+  }
+  return ok == 1;
+}
+
 cudaError_t launch_cluster_select(const DecWs& d, const IndexerArgs& a, int* dev_status, cudaStream_t st) {
   const int n = a.q_pos0 + 1;                    // one row per sequence (T = 1)
   const size_t smem = sizeof(ClusterSelSmem);
@@ -781,7 +804,7 @@ cudaError_t launch_indexer_decode(const IndexerArgs& a, void* ws, size_t ws_byte
   if (indexer_decode_tc_supported(a)) {
     size_t need = 0;
     const DecWs d = carve_ws(ws, a.B * a.T, a.S, &need);
-    if (ws_bytes >= need) {
+    if (ws_bytes >= need && cluster_select_ok()) {
       // histogram built by the scorer, then the clustered select
       // rows * HBINS ints: a whole number of 16-byte words (HBINS is a multiple of 4)
       const size_t n16 = static_cast<size_t>(a.B) * a.T * HBINS / 4;

@@ -692,7 +692,34 @@ bool sparse_attn_tc_cluster_merge(const AttnArgs& a, int nsplit) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
   const long long items = static_cast<long long>(a.B) * a.T * nsplit;
-  return nsplit > 1 && nsplit <= kTcMaxClusterSplit && items <= n_sm;
+  if (nsplit < 2 || nsplit > kTcMaxClusterSplit || items > n_sm) return false;
+  // clusters of nsplit CTAs with this shared memory must fit the device
+  // (asked once per size and process)
+  static int fits[kTcMaxClusterSplit + 1] = {-1, -1, -1, -1, -1, -1, -1, -1, -1};
+  if (fits[nsplit] < 0) {
+    int v = 0, n = 0;
+    const size_t smem = sizeof(AttnTcSmem) + 1024;
+    cudaError_t q = cudaFuncSetAttribute(sparse_attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (q == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(nsplit));
+      cfg.blockDim = dim3(NTHREADS);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = static_cast<unsigned>(nsplit);
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      q = cudaOccupancyMaxActiveClusters(&n, sparse_attn_tc_kernel<true>, &cfg);
+      if (q == cudaSuccess && n > 0) v = 1;
+    }
+    if (q != cudaSuccess) cudaGetLastError();    // a refused query leaves no error behind
+    fits[nsplit] = v;
+  }
+  return fits[nsplit] == 1;
 }
 
 }  // namespace ic
