@@ -42,22 +42,19 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int n
   }
   if (lane == 31) warp_sums[wid] = incl;
   sync();
-  if (wid == 0) {
-    int s = lane < nw ? warp_sums[lane] : 0;
-    int si = s;
+  // every warp scans the warp totals itself (no second round through
+  // shared memory); the barrier after lets the next scan reuse warp_sums
+  const int s = lane < nw ? warp_sums[lane] : 0;
+  int si = s;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int t = __shfl_up_sync(0xffffffffu, si, o);
-      if (lane >= o) si += t;
-    }
-    if (lane < nw) warp_sums[lane] = si - s;   // exclusive prefix of warps
-    if (lane == 31) warp_sums[31] = si;        // grand total (nw <= 31)
+  for (int o = 1; o < 32; o <<= 1) {
+    int t = __shfl_up_sync(0xffffffffu, si, o);
+    if (lane >= o) si += t;
   }
+  total = __shfl_sync(0xffffffffu, si, 31);
+  const int before = __shfl_sync(0xffffffffu, si - s, wid);
   sync();
-  total = warp_sums[31];
-  int r = warp_sums[wid] + incl - v;
-  sync();
-  return r;
+  return before + incl - v;
 }
 
 // Mask of the top `bits` bits of a word (0 <= bits <= 32).
