@@ -583,7 +583,7 @@ __device__ void cut_bin_to_out(const uint32_t* key, const int* pos, int n, int k
   for (int j = tot + tid; j < k; j += STHREADS) out[j] = -1;
 }
 
-struct __align__(128) ClusterSelSmem {
+struct __align__(16) ClusterSelSmem {
   float buf[SPASS];                      // a pass of this CTA's part of the score row
   uint32_t key[FCAP];
   int pos[FCAP];
@@ -594,8 +594,8 @@ struct __align__(128) ClusterSelSmem {
 
 __global__ void __cluster_dims__(SCL, 1, 1) __launch_bounds__(STHREADS)
 select_cluster_kernel(const float* scores, size_t pitch, const int* hist, int32_t* idx, int n, int k, int* status) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  ClusterSelSmem& sm = *reinterpret_cast<ClusterSelSmem*>(smem_raw);
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  ClusterSelSmem& sm = *reinterpret_cast<ClusterSelSmem*>(smem_raw);   // bulk copies need 16-byte alignment
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
   const int row = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
