@@ -598,7 +598,7 @@ select_cluster_kernel(const float* scores, size_t pitch, const int* hist, int32_
   ClusterSelSmem& sm = *reinterpret_cast<ClusterSelSmem*>(smem_raw);   // bulk copies need 16-byte alignment
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
-  const int row = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int row = blockIdx.y, tid = threadIdx.x;
   if (tid == 0) {
     tc::mbar_init(&sm.bar, 1);
     tc::fence_mbar_init();
