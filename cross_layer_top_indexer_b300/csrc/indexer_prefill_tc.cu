@@ -61,7 +61,7 @@ constexpr int DD = 128;                  // indexer feature dim
 constexpr int NCOL = QPB * HH;           // MMA N = 256
 constexpr int KT = 128;                  // keys per tile (MMA M)
 constexpr int KSTAGES = 4;               // ring of K-half tiles (16 KB each)
-constexpr int CAP = kMaxK + 768;         // candidate slots per row
+constexpr int CAP = kMaxK + 896;         // candidate slots per row (what shared memory leaves: 227 KB in all)
 constexpr int WG_THREADS = 128;
 constexpr int SEG = CAP / WG_THREADS;    // entries per thread in a cut
 // A cut keeps at most this many: close to k, so that the threshold it leaves
