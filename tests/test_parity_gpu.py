@@ -291,11 +291,13 @@ def test_decode_select_ties(S, n_top, top_val):
         pu.check_topk(got[b], pu.to_f64(q[b]), pu.to_f64(kI[b]), pu.to_f64(w[b]), k, S - 1, [0], exact=True)
 
 
-def test_decode_select_paths_agree():
+@pytest.mark.parametrize("S", [40000, 300007])
+def test_decode_select_paths_agree(S):
     # the clustered select (workspace with the histogram) and
-    # the one-CTA select (workspace of the score rows only) pick the same rows
+    # the one-CTA select (workspace of the score rows only) pick the same rows;
+    # at 300007 keys each CTA of a cluster copies and lists its quarter of the
+    # row in three passes, the last one ragged
     dc = synth.DECODE.with_(B=3)
-    S = 40000
     q, kI, ks, w = synth.make_indexer_inputs(dc, 0, 23, DEV, T=1, S=S)
     full = _idx64(B.indexer_topk(q, kI, w, 2048, S - 1, kscale=ks, S=S))
     small_ws = torch.empty(3 * ((S + 3) // 4) * 4 * 4, dtype=torch.uint8, device=DEV)
