@@ -222,6 +222,7 @@ def test_indexer_constant_scores_lowest_positions(H, D):
     (2, 3, 4003, 4100, 4000, 16, "bf16"),
     (3, 1, 100, 100, 99, 2048, "bf16"),      # fewer causal keys than k
     (1, 8, 3008, 3008, 3000, 500, "e4m3"),
+    (2, 1, 2049, 2100, 2048, 2048, "e4m3"),  # one key more than k: a cut of one, 4-CTA clusters of ~512 keys
 ])
 def test_indexer_decode_path(Bn, T, S, S_cap, q_pos0, k, kd):
     cfg = synth.StackConfig("dec", 1, "F", Bn, T, S, 64, 128, k, 32, 128, kd, "normal", q_pos0)
